@@ -1,0 +1,476 @@
+"""Benchmark of the fused reduce + bias/residual add + RMSNorm + quant stage on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload NAME|INDEX] [--no-extras]
+
+A step is one call of the whole per-token stage (sum of tp partials, bias + residual add, new
+residual, RMSNorm, output in the workload's form, padding rows zeroed) over one batch of
+synthetic, seeded input already resident in HBM. The default workload is tp=4, 4093 tokens padded
+to 4096, H=4096, bf16 output. The timed loop rotates over several input/output sets whose total
+size is far above the 129 MB L2, so every step reads its inputs from HBM.
+
+Printed: one JSON line (rank 0) with the headline HBM GB/s (algorithmic bytes / time), Mtokens/s,
+the roofline of the kernel against the measured HBM copy peak, the end-to-end figure through the
+public API with host buffers (host->device copies and device->host reads in the timed region),
+the oracle timed on the host cores as a CPU baseline, SM clocks sampled during the timed region,
+and per-workload figures for the other four workloads.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU (independent replicas;
+nothing is exchanged between ranks) and the value is the sum over ranks divided by the slowest
+rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "fused reduce+add-RMSNorm+quant HBM GB/s and Mtokens/s; % of GB300 HBM peak"
+DEFAULT_WORKLOAD = "tp4_T4093p4096_H4096_bf16"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ------------------------------------------------------------------------------ workload math
+def algorithmic_bytes(tp: int, T_valid: int, T_pad: int, H: int, mode: str,
+                      residual: bool = True) -> int:
+    """Bytes one call must move: per valid row tp partial rows + the residual row read (2H each)
+    and residual_out + out (+ scales) written; per padding row the zero writes only. Weight and
+    bias (2H each, read once per CTA and L2-resident) are left out."""
+    out_row = {"none": 2 * H, "fp8_static": H, "fp8_per_token": H + 4,
+               "nvfp4": H // 2 + H // 16}[mode]
+    read_row = 2 * H * (tp + (1 if residual else 0))
+    write_row = 2 * H + out_row
+    return T_valid * (read_row + write_row) + (T_pad - T_valid) * write_row
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in sorted(os.listdir(os.path.join(ROOT, "sequence_reduce_add_gb300", "csrc"))):
+        with open(os.path.join(ROOT, "sequence_reduce_add_gb300", "csrc", rel), "rb") as f:
+            h.update(rel.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peak() -> tuple[float, str]:
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(workload: str) -> int | None:
+    """DRAM bytes per launch from a committed ncu capture of the current kernel sources."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "ncu_traffic.json")) as f:
+            data = json.load(f)
+    except Exception:
+        return None
+    entry = data.get(workload)
+    if not entry or entry.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    return int(entry["dram_bytes_per_launch"])
+
+
+# ------------------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi samples (200 ms) of SM clock and throttle reasons while running."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._reader = threading.Thread(target=self._read, daemon=True)
+            self._reader.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self, t_start: float, t_end: float) -> dict:
+        del t_start, t_end
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------ our arm
+class Problem:
+    """One resident input/output set of a workload, with prebuilt C-ABI argument tuples."""
+
+    def __init__(self, w: dict, seed: int, device, sp):
+        from sequence_reduce_add_gb300 import synth
+        self.inp = synth.make_inputs(w, seed=seed, device=device)
+        i = self.inp
+        self.outs = sp.allocate_outputs(i["T_pad"], i["H"], i["mode"], device)
+        self.scale = (torch.tensor([i["scale"]], dtype=torch.float32, device=device)
+                      if i["scale"] is not None else None)
+        p = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+        self.args = (p(i["partials"]), i["tp"], i["T_pad"], i["T_valid"], i["H"], p(i["residual"]),
+                     p(i["weight"]), p(i["bias"]), ctypes.c_float(i["eps"]),
+                     sp.QUANT_MODES[i["mode"]], p(self.scale), p(self.outs["out"]),
+                     p(self.outs["out_scales"]), p(self.outs["residual_out"]))
+
+    def nbytes(self) -> int:
+        ts = [self.inp["partials"], self.inp["residual"], self.outs["out"],
+              self.outs["out_scales"], self.outs["residual_out"]]
+        return sum(t.numel() * t.element_size() for t in ts if t is not None)
+
+
+def time_kernel_loop(lib, problems, steps: int, stream, per_launch_events: bool):
+    """Launch `steps` calls rotating over `problems` on `stream`; returns (total_ms, [launch ms])."""
+    handle = ctypes.c_void_p(stream.cuda_stream)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(steps)] if per_launch_events else None)
+    fn = lib.sp_fused_reduce_norm
+    n = len(problems)
+    start.record(stream)
+    for s in range(steps):
+        if ev:
+            ev[s][0].record(stream)
+        st = fn(*problems[s % n].args, handle)
+        if st != 0:
+            raise RuntimeError(f"sp_fused_reduce_norm returned {st}")
+        if ev:
+            ev[s][1].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    total = start.elapsed_time(end)
+    launches = [a.elapsed_time(b) for a, b in ev] if ev else []
+    return total, launches
+
+
+def e2e_loop(sp, w: dict, problem: Problem, steps: int, warmup: int, stream) -> dict:
+    """The same call through the public API with host buffers: each step copies the step's
+    inputs from pinned host memory to the device, runs the stage, and reads every output back
+    into pinned host memory."""
+    i, o = problem.inp, problem.outs
+    host_in = {k: i[k].cpu().pin_memory() for k in ("partials", "residual", "weight", "bias")
+               if i[k] is not None}
+    host_out = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in o.items()
+                if v is not None}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in host_out.values())
+
+    def step():
+        with torch.cuda.stream(stream):
+            for k, t in host_in.items():
+                i[k].copy_(t, non_blocking=True)
+            sp.sp_fused_reduce_norm(i["partials"], i["weight"], o["out"], o["residual_out"],
+                                    residual=i["residual"], bias=i["bias"], eps=i["eps"],
+                                    quant_mode=i["mode"], scale=problem.scale,
+                                    out_scales=o["out_scales"], T_valid=i["T_valid"],
+                                    stream=stream)
+            for k, t in host_out.items():
+                t.copy_(o[k], non_blocking=True)
+
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(steps):
+        step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    return {"ms_per_step": ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "host_inputs": host_in}
+
+
+class OracleRunner:
+    """The oracle as it stands, on row samples of one workload, on all host cores."""
+
+    def __init__(self, w: dict, host_in: dict):
+        import oracle
+        from sequence_reduce_add_gb300 import synth
+        b = synth.bf16_bits
+        self.oracle = oracle
+        self.w = w
+        self.parts = b(host_in["partials"])
+        self.res = b(host_in["residual"]) if "residual" in host_in else None
+        self.wt = b(host_in["weight"])
+        self.bs = b(host_in["bias"]) if "bias" in host_in else None
+        self.scale = host_in.get("scale")
+        self.cores = os.cpu_count() or 1
+        self.buffers = None
+        self.next_row = 0
+
+    def run(self, nrows: int) -> tuple[float, int]:
+        """Compute `nrows` valid rows (cycling through the workload); returns (seconds, bytes)."""
+        Tv = self.w["T_valid"]
+        nrows = max(1, min(nrows, Tv))
+        if self.next_row + nrows > Tv:
+            self.next_row = 0
+        rows = (self.next_row, self.next_row + nrows)
+        self.next_row += nrows
+        t0 = time.perf_counter()
+        r = self.oracle.fused_reduce_norm(self.parts, self.res, self.wt, self.bs, 1e-6,
+                                          self.w["mode"], self.scale, Tv, rows=rows,
+                                          threads=self.cores, buffers=self.buffers)
+        dt = time.perf_counter() - t0
+        assert r["status"] == 0
+        self.buffers = r
+        tp, _, H = self.parts.shape
+        return dt, algorithmic_bytes(tp, nrows, nrows, H, self.w["mode"], self.res is not None)
+
+    def rows_for(self, seconds: float) -> int:
+        probe = min(self.w["T_valid"], max(self.cores, 32))
+        dt, _ = self.run(probe)
+        return max(1, int(probe * seconds / max(dt, 1e-6)))
+
+
+def cpu_baseline(w: dict, host_in: dict, target_s: float = 12.0) -> dict:
+    """The oracle as it stands, on a bounded row sample of the workload, on all host cores."""
+    runner = OracleRunner(w, host_in)
+    n = runner.rows_for(target_s)
+    runner.next_row = 0
+    t, nbytes = runner.run(n)
+    n = min(n, w["T_valid"])
+    return {"value": nbytes / t / 1e9, "unit": "GB/s", "cores": runner.cores, "kind": "oracle",
+            "sample": f"rows 0..{n - 1} of {w['T_valid']} valid rows "
+                      f"({nbytes / 1e6:.1f} MB algorithmic), {runner.cores} threads, {t:.1f} s",
+            "mtokens_per_s": n / t / 1e6}
+
+
+def run_ours(args) -> None:
+    import sequence_reduce_add_gb300 as sp
+    from sequence_reduce_add_gb300 import build as sp_build
+    from sequence_reduce_add_gb300 import synth
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=device)
+    if rank == 0 or world == 1:
+        sp_build.build()
+    if dist:
+        dist.barrier()
+    lib = sp.load_library()
+
+    w = synth.workload(args.workload if not str(args.workload).isdigit() else int(args.workload))
+    one = algorithmic_bytes(w["tp"], w["T_valid"], w["T_pad"], w["H"], w["mode"])
+    # enough resident sets that one full rotation is far above L2
+    probe = Problem(w, synth.BASE_SEED + 1 + synth.WORKLOADS.index(
+        next(x for x in synth.WORKLOADS if x["name"] == w["name"])), device, sp)
+    sets = max(2, min(8, -(-(4 * L2_BYTES) // probe.nbytes())))
+    problems = [probe] + [Problem(w, probe.inp["seed"] + 1000 * k, device, sp)
+                          for k in range(1, sets)]
+    rotation_bytes = sum(p.nbytes() for p in problems)
+    stream = torch.cuda.Stream(device=device)
+
+    # warm-up, then the timed region (barrier + synchronize on both sides)
+    time_kernel_loop(lib, problems, max(args.warmup, 3), stream, False)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t0 = time.time()
+        total_ms, launch_ms = time_kernel_loop(lib, problems, args.steps, stream, True)
+        t1 = time.time()
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+        t = torch.tensor([total_ms], device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = one * args.steps * world / (total_ms / 1e3) / 1e9
+    mtok = w["T_valid"] * args.steps * world / (total_ms / 1e3) / 1e6
+    kernel_ms = float(np.mean(launch_ms))
+    peak, peak_kind = measured_peak()
+    achieved = one / (kernel_ms / 1e3) / 1e9
+
+    e2e = e2e_loop(sp, w, problems[0], steps=max(5, min(50, args.steps // 100)),
+                   warmup=2, stream=stream)
+    host_in = e2e.pop("host_inputs")
+    if problems[0].inp["scale"] is not None:
+        host_in["scale"] = problems[0].inp["scale"]
+    e2e_value = one / (e2e["ms_per_step"] / 1e3) / 1e9
+
+    extras = {}
+    if not args.no_extras:
+        for other in synth.WORKLOADS:
+            if other["name"] == w["name"]:
+                continue
+            extras[other["name"]] = bench_extra(lib, sp, synth, other, device, stream, peak)
+
+    if rank != 0:
+        return
+    cpu = cpu_baseline(w, host_in) if world == 1 or rank == 0 else None
+    cfg = sp.sp_select_launch(w["tp"], w["T_pad"], w["H"], w["mode"]).as_dict()
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 6),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded; bf16 inputs as in the workload definition)",
+        "mtokens_per_s": round(mtok, 3),
+        "config": {"workload": w["name"], "tp": w["tp"], "T_valid": w["T_valid"],
+                   "T_pad": w["T_pad"], "H": w["H"], "quant": w["mode"],
+                   "bytes_per_step": one, "launch": cfg,
+                   "l2": f"inputs larger than L2: {len(problems)} resident sets rotated, "
+                         f"{rotation_bytes / 1e6:.0f} MB per rotation (L2 129 MB)",
+                   "parallelism": f"replicas x{world}"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
+                     "traffic": ncu_traffic(w["name"]), "kernel_ms": round(kernel_ms, 6),
+                     "kernel": "k_staged" if cfg["kernel"] == 0 else "k_direct"},
+        "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
+                "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
+                "ms_per_step": round(e2e["ms_per_step"], 4)},
+        "cpu_baseline": cpu,
+        "clocks": clocks.summary(t0, t1),
+        "gpu_launches": args.steps,
+        "workloads": extras,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def bench_extra(lib, sp, synth, w, device, stream, peak) -> dict:
+    """Per-workload kernel figures for the other workloads (rotating sets, CUDA events)."""
+    base = Problem(w, synth.BASE_SEED + 1 + synth.WORKLOADS.index(w), device, sp)
+    sets = max(2, min(6, -(-(4 * L2_BYTES) // base.nbytes())))
+    problems = [base] + [Problem(w, base.inp["seed"] + 1000 * k, device, sp)
+                         for k in range(1, sets)]
+    one = algorithmic_bytes(w["tp"], w["T_valid"], w["T_pad"], w["H"], w["mode"])
+    steps = max(20, int(0.25e9 / max(one, 1)) * 4)
+    steps = min(steps, 4000)
+    time_kernel_loop(lib, problems, 10, stream, False)
+    total, launches = time_kernel_loop(lib, problems, steps, stream, True)
+    k = float(np.mean(launches))
+    gbs = one / (k / 1e3) / 1e9
+    res = {"GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+           "mtokens_per_s": round(w["T_valid"] / (k / 1e3) / 1e6, 3), "kernel_us": round(k * 1e3, 2),
+           "step_us": round(total / steps * 1e3, 2), "steps": steps, "bytes": one,
+           "sets": len(problems)}
+    del problems
+    torch.cuda.empty_cache()
+    return res
+
+
+# ------------------------------------------------------------------------------ reference arm
+def run_reference(args) -> None:
+    """The oracle (fp64 C++ on the host cores), timed as the reference arm on our workload.
+
+    Each step computes a bounded sample of rows of the workload, sized so that the whole
+    --warmup W --steps K run takes about --reference-budget-s seconds."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from oracle import build as oracle_build
+    from sequence_reduce_add_gb300 import synth
+    oracle_build.build()
+    w = synth.workload(args.workload if not str(args.workload).isdigit() else int(args.workload))
+    inp = synth.make_inputs(w, device="cpu")
+    host_in = {k: inp[k] for k in ("partials", "residual", "weight", "bias") if inp[k] is not None}
+    if inp["scale"] is not None:
+        host_in["scale"] = inp["scale"]
+    runner = OracleRunner(w, host_in)
+    total_steps = max(args.warmup, 0) + args.steps
+    rows = runner.rows_for(args.reference_budget_s / max(total_steps, 1))
+    for _ in range(max(args.warmup, 0)):
+        runner.run(rows)
+    secs, nbytes = 0.0, 0
+    for _ in range(args.steps):
+        dt, b = runner.run(rows)
+        secs += dt
+        nbytes += b
+    value = nbytes / secs / 1e9
+    tok = min(rows, w["T_valid"]) * args.steps
+    one = algorithmic_bytes(w["tp"], w["T_valid"], w["T_pad"], w["H"], w["mode"])
+    cpu = {"value": round(value, 4), "unit": "GB/s", "cores": runner.cores, "kind": "oracle",
+           "sample": f"{min(rows, w['T_valid'])} rows of {w['T_valid']} per step, "
+                     f"{args.steps} timed steps, {secs:.1f} s, {runner.cores} threads"}
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic (seeded)", "mtokens_per_s": round(tok / secs / 1e6, 4),
+        "config": {"workload": w["name"], "tp": w["tp"], "T_valid": w["T_valid"],
+                   "T_pad": w["T_pad"], "H": w["H"], "quant": w["mode"], "bytes_per_step": one,
+                   "l2": "host run (no GPU)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main() -> None:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--reference-budget-s", type=float, default=60.0,
+                    help="CPU seconds for the whole reference-arm run (bounded row samples)")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,200 @@
+/*
+ * sp_fused.h — C boundary of the GB300 (sm_103a) library for the per-token stage of the
+ * sequence-parallel rewrite
+ *
+ *     AllReduce -> RMSNorm -> quant   ==>   ReduceScatter -> RMSNorm -> quant -> AllGather
+ *
+ * On one GPU the tp partial-sum tensors that a ReduceScatter would reduce are plain device
+ * buffers; the library sums them, adds bias and residual, applies RMSNorm with a weight, writes
+ * the new residual and emits bf16, FP8-E4M3 (static per-tensor or per-token dynamic) or NVFP4
+ * output, with padding rows zeroed. Output rows are in token order, which on one device is the
+ * shard-contiguous layout an AllGather along the token dimension would produce.
+ *
+ * Sources (web pages; cited by title and section):
+ *   "vllm-ascend SP / FlashComm1 / FlashComm2" (ai6s.net): §2.1 the AR -> RS + norm + AG rewrite;
+ *       §2.2 its mathematical equivalence; §2.3 the add-RMSNorm-bias pattern and its replacement
+ *       (reduce_scatter, chunk the residual, add + RMSNorm with weight and bias slot, all_gather);
+ *       §2.4 token count padded to a multiple of tp; §3.3 pad -> reduce_scatter(dim 0) ... ->
+ *       all_gather(dim 0) -> unpad.
+ *   "vLLM SP / AsyncTP / quantization tech notes" (beaiera.top): §四 the static FP8 and NVFP4
+ *       patterns (RS -> RMSNorm(local) -> quant(local) -> AG) and the per-tensor correctness
+ *       table (static per-tensor, per-token and per-block scales are shard-local; dynamic
+ *       per-tensor is not).
+ *   "vllm-ascend PR #18671 解读: GLM V1 SP layout through DSA-CP": §2 contiguous token shards
+ *       (3500 tokens padded to 3504, 219 per rank at TP=16); §5.2 shard checks that raise on a
+ *       mismatch and zeroing of padding rows; §5.3 tail padding rows zeroed after the reduction.
+ *   "基于Atlas A3集群的LongCat-Flash模型推理性能优化实践": o_proj TP paragraph (reduce_scatter =
+ *       element-wise sum, then split along the batch/token dimension).
+ *
+ * Conventions for every entry point:
+ *   - All tensor arguments are DEVICE pointers into the memory of the current CUDA device, unless
+ *     the argument says "host". The caller owns every buffer; the library allocates nothing, keeps
+ *     no per-call state and may be called concurrently from several host threads.
+ *   - bf16 is IEEE binary32's top 16 bits; FP8 E4M3 is the OCP "E4M3" (fn) format; E2M1 is the
+ *     OCP MX FP4 format. All tensors are dense, row-major, C-contiguous.
+ *   - Calls are asynchronous on `stream` (NULL = legacy default stream); nothing synchronises the
+ *     host. Errors found before the launch leave every buffer untouched.
+ */
+#ifndef SP_FUSED_H
+#define SP_FUSED_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t, so CUDA callers pass their stream directly. */
+typedef struct CUstream_st* sp_stream_t;
+
+typedef enum sp_status {
+  SP_OK = 0,
+  SP_ERR_INVALID_ARG = 1,  /* a shape, mode, eps, pointer or overlap rule is broken */
+  SP_ERR_UNSUPPORTED = 2,  /* well-formed but not provided (dynamic per-tensor FP8; H too large) */
+  SP_ERR_ALIGNMENT = 3,    /* a device pointer is not 16-byte aligned */
+  SP_ERR_CUDA = 4          /* the CUDA runtime reported an error (launch or attribute query) */
+} sp_status;
+
+typedef enum sp_quant_mode {
+  SP_QUANT_NONE = 0,             /* out: bf16 [T_pad][H] */
+  SP_QUANT_FP8_STATIC = 1,       /* out: e4m3 [T_pad][H]; q = E4M3(y / scale[0]) */
+  SP_QUANT_FP8_PER_TOKEN = 2,    /* out: e4m3 [T_pad][H]; out_scales: fp32 [T_pad], s_t = max|y_t|/448 */
+  SP_QUANT_NVFP4 = 3,            /* out: e2m1 packed [T_pad][H/2]; out_scales: e4m3 [T_pad][H/16] */
+  SP_QUANT_FP8_DYNAMIC_PER_TENSOR = 4 /* always SP_ERR_UNSUPPORTED: its scale is not shard-local */
+} sp_quant_mode;
+
+/*
+ * sp_fused_reduce_norm — the whole per-token stage in one pass over HBM.
+ *
+ * For every row t < T_valid (h, y are fp32 vectors of length H):
+ *   h            = sum_{r<tp} partials[r][t] + bias + residual[t]     (the ReduceScatter sum)
+ *   residual_out[t] = bf16_rn(h)                                      (the new residual)
+ *   y            = h * rsqrt(mean(h^2) + eps) * weight                  (RMSNorm, per token)
+ *   out[t]       = by quant_mode:
+ *     NONE           bf16_rn(y)
+ *     FP8_STATIC     e4m3_satfinite_rn(y / scale[0])        (scale = dequantisation scale)
+ *     FP8_PER_TOKEN  s_t = max_j|y_j| / 448 -> out_scales[t] (fp32);
+ *                    e4m3_satfinite_rn(y / s_t), all zero when s_t == 0
+ *     NVFP4          per 16-element block b of the row: sf_b = e4m3_satfinite_rn(gs * max|y_b| / 6)
+ *                    -> out_scales[t][b]; q = e2m1_satfinite_rn(y * gs / sf_b), zero when
+ *                    sf_b == 0; gs = scale[0] (an encode multiplier); element 2i of the row goes
+ *                    to the low nibble of byte i, 2i+1 to the high nibble.
+ * Rows t >= T_valid are padding: none of their inputs is read and every byte of their out,
+ * out_scales and residual_out rows is written as zero.
+ *
+ * Arguments:
+ *   partials     bf16 [tp][T_pad][H]: partial r holds rank r's un-reduced output for every token.
+ *   tp           number of partials, >= 1.
+ *   T_pad        padded token count, a multiple of tp (shard r = rows [r*T_pad/tp, (r+1)*T_pad/tp)).
+ *   T_valid      real tokens, 0 <= T_valid <= T_pad.
+ *   H            hidden size, > 0, multiple of 8 (of 16 for NVFP4), at most sp_max_hidden().
+ *   residual     bf16 [T_pad][H], or NULL for a first layer with no incoming residual.
+ *   weight       bf16 [H] RMSNorm weight.
+ *   bias         bf16 [H] added once after the reduction, or NULL.
+ *   eps          > 0 and finite.
+ *   quant_mode   an sp_quant_mode.
+ *   scale        device pointer to one fp32: the static FP8 scale (> 0) or the NVFP4 global
+ *                scale gs (> 0); may be NULL for NONE and FP8_PER_TOKEN. Its value is read on
+ *                the device and is not checked.
+ *   out          see quant_mode.
+ *   out_scales   NULL for NONE and FP8_STATIC; fp32 [T_pad] for FP8_PER_TOKEN; e4m3
+ *                [T_pad][H/16] (row-major, one byte per block) for NVFP4.
+ *   residual_out bf16 [T_pad][H]; may be exactly `residual` (updated in place), otherwise it
+ *                must not overlap any input.
+ *   stream       CUDA stream of the launch.
+ * Every non-NULL pointer must be 16-byte aligned (SP_ERR_ALIGNMENT). No output may overlap an
+ * input or another output (SP_ERR_INVALID_ARG), except residual_out == residual.
+ * Checks run in this order and the first failure is returned: quant_mode, shapes (tp, T_pad,
+ * T_valid, H), eps, required pointers, overlaps, alignment, H <= sp_max_hidden(). T_pad == 0
+ * is a valid call that launches nothing.
+ * Returns SP_OK once the kernel is enqueued, or the failed check's status, or SP_ERR_CUDA.
+ */
+sp_status sp_fused_reduce_norm(const void* partials, int tp, int64_t T_pad, int64_t T_valid,
+                               int64_t H, const void* residual, const void* weight,
+                               const void* bias, float eps, int quant_mode, const float* scale,
+                               void* out, void* out_scales, void* residual_out,
+                               sp_stream_t stream);
+
+/*
+ * sp_check_args — the argument checks of sp_fused_reduce_norm alone, in the same order and with
+ * the same statuses. Pointers are only compared, never dereferenced; touches no GPU and needs
+ * no CUDA device.
+ */
+sp_status sp_check_args(const void* partials, int tp, int64_t T_pad, int64_t T_valid, int64_t H,
+                        const void* residual, const void* weight, const void* bias, float eps,
+                        int quant_mode, const float* scale, const void* out,
+                        const void* out_scales, const void* residual_out);
+
+/*
+ * Launch configurations. sp_fused_reduce_norm picks one by itself (sp_select_launch tells
+ * which); sp_fused_reduce_norm_with_config runs a given one, for tests and tuning. Every
+ * configuration computes the same function.
+ *   kernel        SP_KERNEL_STAGED: one CTA per row at a time; a producer thread streams the
+ *                 row's tp partial rows and residual row from HBM into a shared-memory ring with
+ *                 bulk asynchronous copies (cp.async.bulk + mbarrier), consumer warps reduce
+ *                 from shared memory. SP_KERNEL_DIRECT: the same CTA-per-row mapping with
+ *                 128-bit loads straight into registers.
+ *   vec_per_thread  16-byte vectors (8 elements) of a row that each consumer thread owns: 1, 2, 4.
+ *   ctas_per_sm     CTAs per SM the grid is sized for: grid = SMs x min(ctas_per_sm, CTAs of
+ *                   this kernel an SM can hold), capped at T_pad; 1 .. 8.
+ *   stages          shared-memory ring depth in row segments of 2*H bytes (STAGED only); 0 picks
+ *                   the deepest ring that fits ctas_per_sm CTAs on an SM.
+ */
+enum { SP_KERNEL_STAGED = 0, SP_KERNEL_DIRECT = 1 };
+
+typedef struct sp_launch_config {
+  int kernel;
+  int vec_per_thread;
+  int ctas_per_sm;
+  int stages;
+} sp_launch_config;
+
+sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
+                           sp_launch_config* config /* host, out */);
+
+sp_status sp_fused_reduce_norm_with_config(const sp_launch_config* config /* host */,
+                                           const void* partials, int tp, int64_t T_pad,
+                                           int64_t T_valid, int64_t H, const void* residual,
+                                           const void* weight, const void* bias, float eps,
+                                           int quant_mode, const float* scale, void* out,
+                                           void* out_scales, void* residual_out,
+                                           sp_stream_t stream);
+
+/*
+ * Layout helpers (host only, no device use).
+ *   sp_pad_tokens: the smallest multiple of tp that is >= T (token padding before the
+ *       ReduceScatter; vllm-ascend SP notes §2.4, §3.3), or -1 if T < 0 or tp < 1.
+ *   sp_shard_rows: rows [*start, *start + *len) of shard `rank` — the contiguous segment of
+ *       T_pad/tp rows that rank owns (PR #18671 notes §2, §5.2); SP_ERR_INVALID_ARG when
+ *       T_pad % tp != 0 or rank is out of range.
+ *   sp_out_bytes / sp_out_scales_bytes: sizes of `out` and `out_scales` for a mode (0 for no
+ *       buffer), or -1 for an invalid mode.
+ *   sp_max_hidden: the largest H the kernels take.
+ */
+int64_t sp_pad_tokens(int64_t T, int tp);
+sp_status sp_shard_rows(int64_t T_pad, int tp, int rank, int64_t* start /* host */,
+                        int64_t* len /* host */);
+int64_t sp_out_bytes(int64_t T_pad, int64_t H, int quant_mode);
+int64_t sp_out_scales_bytes(int64_t T_pad, int64_t H, int quant_mode);
+int64_t sp_max_hidden(void);
+
+/* Name of a status code, e.g. "SP_ERR_ALIGNMENT"; "SP_UNKNOWN_STATUS" for other values. */
+const char* sp_status_string(int status);
+
+/*
+ * Device-side error word. The staged kernel's waits on its shared-memory ring are bounded in
+ * time; a wait that runs out (which only a hardware or runtime fault could cause) sets
+ * SP_DEVICE_ERR_WAIT_TIMEOUT here, abandons the launch after letting its copies in flight
+ * land, and the row it was on holds undefined values. sp_device_error reads (and, when
+ * `clear` is non-zero, resets) the word of the current device; it synchronises with the
+ * device. SP_ERR_CUDA if the runtime call fails.
+ */
+enum { SP_DEVICE_ERR_WAIT_TIMEOUT = 1 };
+sp_status sp_device_error(uint32_t* flags /* host, out */, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SP_FUSED_H */

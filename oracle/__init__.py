@@ -80,19 +80,28 @@ def out_layout(T_pad: int, H: int, mode: str):
 def fused_reduce_norm(partials: np.ndarray, residual: np.ndarray | None, weight: np.ndarray,
                       bias: np.ndarray | None, eps: float, mode: str, scale: float | None,
                       T_valid: int, *, want_y: bool = False, rows: tuple[int, int] | None = None,
-                      threads: int = 1, lib: ctypes.CDLL | None = None) -> dict:
+                      threads: int = 1, lib: ctypes.CDLL | None = None,
+                      buffers: dict | None = None) -> dict:
     """Run the oracle over rows ``rows`` (default all) of a [tp, T_pad, H] problem.
 
     Returns a dict with ``status``, ``out``, ``out_scales`` (or None), ``residual_out`` and, when
-    ``want_y``, the unrounded fp64 ``y`` [T_pad, H]. Rows outside ``rows`` are left zero.
+    ``want_y``, the unrounded fp64 ``y`` [T_pad, H]. Rows outside ``rows`` are left zero, unless
+    ``buffers`` (a previous result) is given: its arrays are then reused and only ``rows`` of
+    them are rewritten.
     """
     lib = lib or load()
     tp, T_pad, H = partials.shape
     oshape, odt, sshape, sdt = out_layout(T_pad, H, mode)
-    out = np.zeros(oshape, odt)
-    out_scales = np.zeros(sshape, sdt) if sshape else None
-    residual_out = np.zeros((T_pad, H), np.uint16)
-    y = np.zeros((T_pad, H), np.float64) if want_y else None
+    if buffers is not None:
+        out, out_scales = buffers["out"], buffers["out_scales"]
+        residual_out, y = buffers["residual_out"], buffers["y"] if want_y else None
+        assert out.shape == oshape and residual_out.shape == (T_pad, H)
+        assert (out_scales is None) == (sshape is None) and (not want_y or y is not None)
+    else:
+        out = np.zeros(oshape, odt)
+        out_scales = np.zeros(sshape, sdt) if sshape else None
+        residual_out = np.zeros((T_pad, H), np.uint16)
+        y = np.zeros((T_pad, H), np.float64) if want_y else None
     scale_arr = np.array([scale], np.float32) if scale is not None else None
     args = [_ptr(partials, ctypes.c_uint16), tp, T_pad, T_valid, H,
             _ptr(residual, ctypes.c_uint16), _ptr(weight, ctypes.c_uint16),

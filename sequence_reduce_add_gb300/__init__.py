@@ -1,0 +1,231 @@
+"""GB300 (sm_103a) fused reduce + bias/residual add + RMSNorm + quant for sequence parallelism.
+
+The per-token stage of the rewrite AllReduce -> RMSNorm -> quant  ==>  ReduceScatter -> RMSNorm
+-> quant -> AllGather, run on one GPU: the tp partial-sum buffers are summed, bias and residual
+added, RMSNorm applied with a weight, the new residual written, and bf16 / FP8-E4M3 (static or
+per-token) / NVFP4 output produced, with padding rows zeroed (vllm-ascend SP/FlashComm notes
+§2.3; vLLM SP/AsyncTP/quant notes §四; PR #18671 notes §5.2-5.3).
+
+Every computation runs in the CUDA library ``libspfused.so`` (include/sp_fused.h). This module
+only marshals arguments: it turns torch tensors into device pointers and sizes, calls the C
+entry point of the same name, and raises ``SpError`` on a non-OK status. There is no fallback:
+without the built library every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+from . import build as _build
+
+__all__ = [
+    "SpError", "QUANT_MODES", "load_library", "sp_fused_reduce_norm",
+    "sp_fused_reduce_norm_with_config", "sp_check_args", "sp_select_launch", "sp_pad_tokens",
+    "sp_shard_rows", "sp_out_bytes", "sp_out_scales_bytes", "sp_max_hidden", "sp_status_string",
+    "sp_device_error", "allocate_outputs", "LaunchConfig",
+]
+
+QUANT_MODES = {"none": 0, "fp8_static": 1, "fp8_per_token": 2, "nvfp4": 3,
+               "fp8_dynamic_per_tensor": 4}
+STATUS_NAMES = {0: "SP_OK", 1: "SP_ERR_INVALID_ARG", 2: "SP_ERR_UNSUPPORTED",
+                3: "SP_ERR_ALIGNMENT", 4: "SP_ERR_CUDA"}
+KERNELS = {"staged": 0, "direct": 1}
+
+_i64 = ctypes.c_int64
+_vp = ctypes.c_void_p
+
+
+class SpError(RuntimeError):
+    """A non-OK status from the library."""
+
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+class LaunchConfig(ctypes.Structure):
+    """sp_launch_config: kernel (0 staged, 1 direct), vec_per_thread, ctas_per_sm, stages."""
+    _fields_ = [("kernel", ctypes.c_int), ("vec_per_thread", ctypes.c_int),
+                ("ctas_per_sm", ctypes.c_int), ("stages", ctypes.c_int)]
+
+    def as_dict(self) -> dict:
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+_MAIN_ARGS = [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.c_float, ctypes.c_int,
+              _vp, _vp, _vp, _vp]
+
+_lib: ctypes.CDLL | None = None
+
+
+def library_path() -> str:
+    return _build.LIBRARY
+
+
+def load_library() -> ctypes.CDLL:
+    """Load libspfused.so (built by ``__graft_entry__.build()`` / ``build.py``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} is missing "
+                           "(run `python -c 'import __graft_entry__ as g; g.build()'`)")
+    lib = ctypes.CDLL(path)
+    lib.sp_fused_reduce_norm.argtypes = _MAIN_ARGS + [_vp]
+    lib.sp_fused_reduce_norm.restype = ctypes.c_int
+    lib.sp_fused_reduce_norm_with_config.argtypes = [ctypes.POINTER(LaunchConfig)] + _MAIN_ARGS + [_vp]
+    lib.sp_fused_reduce_norm_with_config.restype = ctypes.c_int
+    lib.sp_check_args.argtypes = _MAIN_ARGS
+    lib.sp_check_args.restype = ctypes.c_int
+    lib.sp_select_launch.argtypes = [ctypes.c_int, _i64, _i64, ctypes.c_int,
+                                     ctypes.POINTER(LaunchConfig)]
+    lib.sp_select_launch.restype = ctypes.c_int
+    lib.sp_pad_tokens.argtypes = [_i64, ctypes.c_int]
+    lib.sp_pad_tokens.restype = _i64
+    lib.sp_shard_rows.argtypes = [_i64, ctypes.c_int, ctypes.c_int, ctypes.POINTER(_i64),
+                                  ctypes.POINTER(_i64)]
+    lib.sp_shard_rows.restype = ctypes.c_int
+    lib.sp_out_bytes.argtypes = [_i64, _i64, ctypes.c_int]
+    lib.sp_out_bytes.restype = _i64
+    lib.sp_out_scales_bytes.argtypes = [_i64, _i64, ctypes.c_int]
+    lib.sp_out_scales_bytes.restype = _i64
+    lib.sp_max_hidden.argtypes = []
+    lib.sp_max_hidden.restype = _i64
+    lib.sp_status_string.argtypes = [ctypes.c_int]
+    lib.sp_status_string.restype = ctypes.c_char_p
+    lib.sp_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
+    lib.sp_device_error.restype = ctypes.c_int
+    _lib = lib
+    return lib
+
+
+def _mode(quant_mode) -> int:
+    return QUANT_MODES[quant_mode] if isinstance(quant_mode, str) else int(quant_mode)
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> int | None:
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    return stream if isinstance(stream, int) else stream.cuda_stream
+
+
+def _main_args(partials, residual, weight, bias, eps, quant_mode, scale, out, out_scales,
+               residual_out, T_valid):
+    tp, T_pad, H = partials.shape
+    if T_valid is None:
+        T_valid = T_pad
+    return [_ptr(partials), tp, T_pad, T_valid, H, _ptr(residual), _ptr(weight), _ptr(bias),
+            ctypes.c_float(eps), _mode(quant_mode), _ptr(scale), _ptr(out), _ptr(out_scales),
+            _ptr(residual_out)]
+
+
+def sp_fused_reduce_norm(partials, weight, out, residual_out, *, residual=None, bias=None,
+                         eps: float = 1e-6, quant_mode="none", scale=None, out_scales=None,
+                         T_valid: int | None = None, stream=None) -> None:
+    """Enqueue the fused stage (see include/sp_fused.h) on ``stream`` (default: torch's current).
+
+    partials: bf16 CUDA tensor [tp, T_pad, H]; residual: bf16 [T_pad, H] or None; weight, bias:
+    bf16 [H] (bias may be None); scale: fp32 CUDA tensor with one element or None; out,
+    out_scales, residual_out: preallocated CUDA tensors (``allocate_outputs``). T_valid defaults
+    to T_pad.
+    """
+    args = _main_args(partials, residual, weight, bias, eps, quant_mode, scale, out, out_scales,
+                      residual_out, T_valid)
+    st = load_library().sp_fused_reduce_norm(*args, _stream_handle(stream))
+    if st != 0:
+        raise SpError(st, "sp_fused_reduce_norm")
+
+
+def sp_fused_reduce_norm_with_config(config: LaunchConfig | dict, partials, weight, out,
+                                     residual_out, *, residual=None, bias=None, eps: float = 1e-6,
+                                     quant_mode="none", scale=None, out_scales=None,
+                                     T_valid: int | None = None, stream=None) -> None:
+    """Like ``sp_fused_reduce_norm`` with an explicit launch configuration."""
+    if isinstance(config, dict):
+        config = LaunchConfig(**config)
+    args = _main_args(partials, residual, weight, bias, eps, quant_mode, scale, out, out_scales,
+                      residual_out, T_valid)
+    st = load_library().sp_fused_reduce_norm_with_config(ctypes.byref(config), *args,
+                                                         _stream_handle(stream))
+    if st != 0:
+        raise SpError(st, "sp_fused_reduce_norm_with_config")
+
+
+def sp_check_args(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode, scale,
+                  out, out_scales, residual_out) -> int:
+    """The library's argument checks on raw addresses (ints or None); returns the status."""
+    return load_library().sp_check_args(partials, tp, T_pad, T_valid, H, residual, weight, bias,
+                                        ctypes.c_float(eps), _mode(quant_mode), scale, out,
+                                        out_scales, residual_out)
+
+
+def sp_select_launch(tp: int, T_pad: int, H: int, quant_mode="none") -> LaunchConfig:
+    cfg = LaunchConfig()
+    st = load_library().sp_select_launch(tp, T_pad, H, _mode(quant_mode), ctypes.byref(cfg))
+    if st != 0:
+        raise SpError(st, "sp_select_launch")
+    return cfg
+
+
+def sp_pad_tokens(T: int, tp: int) -> int:
+    return load_library().sp_pad_tokens(T, tp)
+
+
+def sp_shard_rows(T_pad: int, tp: int, rank: int) -> tuple[int, int]:
+    start, length = _i64(), _i64()
+    st = load_library().sp_shard_rows(T_pad, tp, rank, ctypes.byref(start), ctypes.byref(length))
+    if st != 0:
+        raise SpError(st, "sp_shard_rows")
+    return start.value, length.value
+
+
+def sp_out_bytes(T_pad: int, H: int, quant_mode) -> int:
+    return load_library().sp_out_bytes(T_pad, H, _mode(quant_mode))
+
+
+def sp_out_scales_bytes(T_pad: int, H: int, quant_mode) -> int:
+    return load_library().sp_out_scales_bytes(T_pad, H, _mode(quant_mode))
+
+
+def sp_max_hidden() -> int:
+    return load_library().sp_max_hidden()
+
+
+def sp_status_string(status: int) -> str:
+    return load_library().sp_status_string(status).decode()
+
+
+def sp_device_error(clear: bool = True) -> int:
+    flags = ctypes.c_uint32()
+    st = load_library().sp_device_error(ctypes.byref(flags), 1 if clear else 0)
+    if st != 0:
+        raise SpError(st, "sp_device_error")
+    return flags.value
+
+
+def allocate_outputs(T_pad: int, H: int, quant_mode, device, residual_out: bool = True) -> dict:
+    """Uninitialised output tensors for a call: ``out``, ``out_scales`` (or None) and
+    ``residual_out`` (the kernel writes every byte of each)."""
+    import torch
+    mode = _mode(quant_mode)
+    if mode == 0:
+        out = torch.empty((T_pad, H), dtype=torch.bfloat16, device=device)
+    elif mode in (1, 2):
+        out = torch.empty((T_pad, H), dtype=torch.uint8, device=device)
+    elif mode == 3:
+        out = torch.empty((T_pad, H // 2), dtype=torch.uint8, device=device)
+    else:
+        raise ValueError(f"unsupported quant mode {quant_mode}")
+    scales = None
+    if mode == 2:
+        scales = torch.empty((T_pad,), dtype=torch.float32, device=device)
+    elif mode == 3:
+        scales = torch.empty((T_pad, H // 16), dtype=torch.uint8, device=device)
+    res = torch.empty((T_pad, H), dtype=torch.bfloat16, device=device) if residual_out else None
+    return {"out": out, "out_scales": scales, "residual_out": res}

@@ -1,0 +1,440 @@
+// sp_device.cuh — device-side building blocks of the fused reduce + add + RMSNorm + quant
+// kernels for sm_103a: 128-bit streaming loads/stores, bf16 unpacking, hardware conversions to
+// bf16x2 / e4m3x2 / e2m1x2, mbarrier and bulk-copy primitives, the per-row block reduction and
+// the per-row epilogue (new residual, RMSNorm, quantisation, stores).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace spk {
+
+enum { kModeNone = 0, kModeFp8Static = 1, kModeFp8PerToken = 2, kModeNvfp4 = 3 };
+
+// A wait on a shared-memory barrier gives up after this long (ns of %globaltimer); between
+// checks a waiting thread sleeps inside mbarrier.try_wait for at most kWaitSleepHintNs.
+constexpr uint64_t kWaitLimitNs = 2000000000ull;
+constexpr uint32_t kWaitSleepHintNs = 100000u;
+
+// Set (atomicOr) by a kernel whose bounded wait ran out; read by sp_device_error().
+__device__ unsigned int g_error_flags = 0;
+constexpr unsigned int kErrWaitTimeout = 1u;
+
+struct Params {
+  const uint16_t* partials;   // bf16 [tp][T_pad][H]
+  const uint16_t* residual;   // bf16 [T_pad][H] or null
+  const uint16_t* weight;     // bf16 [H]
+  const uint16_t* bias;       // bf16 [H] or null
+  const float* scale;         // fp32 [1] or null
+  void* out;
+  void* out_scales;
+  uint16_t* residual_out;     // bf16 [T_pad][H]
+  int64_t T_pad;
+  int64_t T_valid;
+  int64_t plane;              // T_pad * H: elements from one partial to the next
+  int H;
+  int nvec;                   // H / 8: 16-byte vectors in a row
+  int tp;
+  int nthreads;               // consumer threads per CTA (a multiple of 32, <= 1024)
+  float eps;
+  int stages;                 // staged kernel: ring depth
+  int seg_stride;             // staged kernel: bytes between ring stages (2H rounded up to 128)
+  int wb_offset;              // staged kernel: byte offset of the weight/bias copy [2][H] bf16
+  int ring_offset;            // staged kernel: byte offset of the ring in dynamic shared memory
+};
+
+// Per-warp slot of the row reduction: sum of squares, max |h*w| and an abort vote.
+struct RedSlot {
+  float ss;
+  float mx;
+  int abort;
+  int pad;
+};
+
+// ---------------------------------------------------------------- global memory
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.L1::no_allocate.L2::256B.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ uint4 ldg_keep(const void* p) {
+  uint4 v;
+  asm("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+      : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+      : "l"(p));
+  return v;
+}
+
+__device__ __forceinline__ void stg_stream(void* p, uint4 v) {
+  asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(v.x), "r"(v.y),
+               "r"(v.z), "r"(v.w)
+               : "memory");
+}
+
+__device__ __forceinline__ void stg_stream(void* p, uint2 v) {
+  asm volatile("st.global.cs.v2.u32 [%0], {%1, %2};" ::"l"(p), "r"(v.x), "r"(v.y) : "memory");
+}
+
+__device__ __forceinline__ void stg_stream(void* p, uint32_t v) {
+  asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// ---------------------------------------------------------------- conversions
+// bf16 -> fp32 is exact: the bf16 pattern is the top half of the binary32 pattern.
+__device__ __forceinline__ void add_bf16x8(const uint4 v, float (&acc)[8]) {
+  acc[0] += __uint_as_float(v.x << 16);
+  acc[1] += __uint_as_float(v.x & 0xFFFF0000u);
+  acc[2] += __uint_as_float(v.y << 16);
+  acc[3] += __uint_as_float(v.y & 0xFFFF0000u);
+  acc[4] += __uint_as_float(v.z << 16);
+  acc[5] += __uint_as_float(v.z & 0xFFFF0000u);
+  acc[6] += __uint_as_float(v.w << 16);
+  acc[7] += __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+__device__ __forceinline__ void unpack_bf16x8(const uint4 v, float (&f)[8]) {
+  f[0] = __uint_as_float(v.x << 16);
+  f[1] = __uint_as_float(v.x & 0xFFFF0000u);
+  f[2] = __uint_as_float(v.y << 16);
+  f[3] = __uint_as_float(v.y & 0xFFFF0000u);
+  f[4] = __uint_as_float(v.z << 16);
+  f[5] = __uint_as_float(v.z & 0xFFFF0000u);
+  f[6] = __uint_as_float(v.w << 16);
+  f[7] = __uint_as_float(v.w & 0xFFFF0000u);
+}
+
+// Round-to-nearest-even to bf16; `lo` lands in the low 16 bits.
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  uint32_t r;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&f)[8]) {
+  return make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]),
+                    pack_bf16x2(f[6], f[7]));
+}
+
+// Four values to E4M3 (round to nearest even, saturating to +-448); value i in byte i.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(a), "f"(b), "f"(c), "f"(d));
+  return r;
+}
+
+// Eight values to E2M1 (round to nearest even, saturating to +-6); value 2i in the low nibble
+// and value 2i+1 in the high nibble of byte i.
+__device__ __forceinline__ uint32_t pack_e2m1x8(const float (&v)[8]) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 b0, b1, b2, b3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b0, %2, %1;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b1, %4, %3;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b2, %6, %5;\n\t"
+      "cvt.rn.satfinite.e2m1x2.f32 b3, %8, %7;\n\t"
+      "mov.b32 %0, {b0, b1, b2, b3};\n\t}"
+      : "=r"(r)
+      : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]));
+  return r;
+}
+
+// One value to its E4M3 code (low byte).
+__device__ __forceinline__ uint32_t e4m3_code(float x) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(0.0f), "f"(x));
+  return r & 0xFFu;
+}
+
+// Exact value of an E4M3 code (every E4M3 value is an fp16 value).
+__device__ __forceinline__ float e4m3_value(uint32_t code) {
+  const uint16_t c16 = static_cast<uint16_t>(code);
+  float f;
+  asm("{\n\t.reg .b32 h2;\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h2, %1;\n\t"
+      "mov.b32 {lo, hi}, h2;\n\t"
+      "cvt.f32.f16 %0, lo;\n\t}"
+      : "=f"(f)
+      : "h"(c16));
+  return f;
+}
+
+// ---------------------------------------------------------------- mbarrier + bulk copy
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` inside the instruction until the
+// phase completes, instead of spinning (spinning warps take issue slots from the producer).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint32_t bar, uint32_t parity,
+                                                    uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase of parity `parity` of barrier `bar` to complete. Gives up (returns false)
+// after kWaitLimitNs, or as soon as *abort is set when `abort` is given.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  const volatile int* abort) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, kWaitSleepHintNs)) return true;
+    if (abort && *abort) return false;
+    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+  }
+}
+
+__device__ __forceinline__ uint64_t l2_evict_first_policy() {
+  uint64_t pol;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+  return pol;
+}
+
+// Bulk asynchronous copy global -> this CTA's shared memory; completion is signalled as
+// `bytes` transactions on barrier `bar`. dst, src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t bytes,
+                                         uint32_t bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+      "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar), "l"(policy)
+      : "memory");
+}
+
+__device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// ---------------------------------------------------------------- row reduction
+// Sum of squares and (optionally) max over the CTA's consumer threads, plus an OR of their abort
+// votes. All consumer threads get bit-identical results (every thread adds the per-warp values
+// in the same order). `slots` holds two sets of 32 per-warp slots used on alternate rows, so one
+// barrier per row suffices.
+template <bool kWithMax>
+__device__ __forceinline__ float2 row_reduce(float ss, float mx, int abort, RedSlot* slots,
+                                             int parity, int nthreads, int* abort_all) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    ss += __shfl_xor_sync(0xFFFFFFFFu, ss, o);
+    if (kWithMax) mx = fmaxf(mx, __shfl_xor_sync(0xFFFFFFFFu, mx, o));
+  }
+  abort = __any_sync(0xFFFFFFFFu, abort);
+  const int warp = threadIdx.x >> 5;
+  RedSlot* s = slots + parity * 32;
+  if ((threadIdx.x & 31) == 0) {
+    s[warp].ss = ss;
+    s[warp].mx = mx;
+    s[warp].abort = abort;
+  }
+  named_barrier_sync(1, nthreads);
+  float tss = 0.0f, tmx = 0.0f;
+  int ab = 0;
+  for (int w = 0; w < (nthreads >> 5); ++w) {
+    tss += s[w].ss;
+    if (kWithMax) tmx = fmaxf(tmx, s[w].mx);
+    ab |= s[w].abort;
+  }
+  *abort_all = ab;
+  return make_float2(tss, tmx);
+}
+
+// ---------------------------------------------------------------- per-row epilogue
+// Constants of the quantiser, read once per thread.
+struct QuantConst {
+  float inv_scale;  // FP8 static: 1 / scale
+  float gs;         // NVFP4: global (encode) scale
+};
+
+template <int kMode>
+__device__ __forceinline__ QuantConst load_quant_const(const Params& p) {
+  QuantConst q{0.0f, 0.0f};
+  if (kMode == kModeFp8Static) q.inv_scale = 1.0f / __ldg(p.scale);
+  if (kMode == kModeNvfp4) q.gs = __ldg(p.scale);
+  return q;
+}
+
+// Zero every output byte of padding row t that this thread owns.
+template <int kVec, int kMode>
+__device__ __forceinline__ void zero_row(const Params& p, int64_t t, int c) {
+  const int64_t H = p.H;
+#pragma unroll
+  for (int k = 0; k < kVec; ++k) {
+    const int v = c + k * p.nthreads;
+    if (v >= p.nvec) continue;
+    stg_stream(p.residual_out + t * H + v * 8, make_uint4(0, 0, 0, 0));
+    if (kMode == kModeNone) {
+      stg_stream(static_cast<uint16_t*>(p.out) + t * H + v * 8, make_uint4(0, 0, 0, 0));
+    } else if (kMode == kModeFp8Static || kMode == kModeFp8PerToken) {
+      stg_stream(static_cast<uint8_t*>(p.out) + t * H + v * 8, make_uint2(0, 0));
+    } else {
+      stg_stream(static_cast<uint8_t*>(p.out) + t * (H / 2) + v * 4, 0u);
+      if ((v & 1) == 0) static_cast<uint8_t*>(p.out_scales)[t * (H / 16) + v / 2] = 0;
+    }
+  }
+  if (kMode == kModeFp8PerToken && c == 0) static_cast<float*>(p.out_scales)[t] = 0.0f;
+}
+
+// Finish row t: h holds sum_r partials + residual + bias for this thread's vectors (zero for
+// vectors past the row). Writes residual_out, normalises, quantises and stores. Returns the
+// CTA-wide abort vote.
+template <int kVec, int kMode>
+__device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)[kVec][8],
+                                          const uint4 (&w)[kVec], const QuantConst& qc,
+                                          RedSlot* slots, int parity, int c, int abort) {
+  const int64_t H = p.H;
+  float ss = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kVec; ++k) {
+    const int v = c + k * p.nthreads;
+    if (v < p.nvec) stg_stream(p.residual_out + t * H + v * 8, pack_bf16x8(h[k]));
+#pragma unroll
+    for (int e = 0; e < 8; ++e) ss += h[k][e] * h[k][e];
+  }
+  // h <- h * w (the weight is applied before the common factor 1/rms)
+  float mx = 0.0f;
+#pragma unroll
+  for (int k = 0; k < kVec; ++k) {
+    float wf[8];
+    unpack_bf16x8(w[k], wf);
+#pragma unroll
+    for (int e = 0; e < 8; ++e) {
+      h[k][e] *= wf[e];
+      if (kMode == kModeFp8PerToken) mx = fmaxf(mx, fabsf(h[k][e]));
+    }
+  }
+  int abort_all = 0;
+  const float2 red =
+      row_reduce<kMode == kModeFp8PerToken>(ss, mx, abort, slots, parity, p.nthreads, &abort_all);
+  const float rinv = rsqrtf(red.x / static_cast<float>(p.H) + p.eps);
+
+  if (kMode == kModeNone) {
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int v = c + k * p.nthreads;
+      float y[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] = h[k][e] * rinv;
+      if (v < p.nvec) stg_stream(static_cast<uint16_t*>(p.out) + t * H + v * 8, pack_bf16x8(y));
+    }
+  } else if (kMode == kModeFp8Static) {
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int v = c + k * p.nthreads;
+      float q[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) q[e] = (h[k][e] * rinv) * qc.inv_scale;
+      if (v < p.nvec)
+        stg_stream(static_cast<uint8_t*>(p.out) + t * H + v * 8,
+                   make_uint2(pack_e4m3x4(q[0], q[1], q[2], q[3]),
+                              pack_e4m3x4(q[4], q[5], q[6], q[7])));
+    }
+  } else if (kMode == kModeFp8PerToken) {
+    // s_t = max|y| / 448 with max|y| = max|h*w| * rinv; the codes are y / s_t = h*w * 448/max|h*w|
+    const float mxhw = red.y;
+    const float s = (mxhw * rinv) / 448.0f;
+    if (c == 0) static_cast<float*>(p.out_scales)[t] = s;
+    float f = 448.0f / mxhw;
+    const bool by_division = !(f <= 3.0e38f);  // max|h*w| is zero or tiny
+    if (s == 0.0f) f = 0.0f;
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int v = c + k * p.nthreads;
+      float q[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e)
+        q[e] = (by_division && s != 0.0f) ? __fdiv_rn(h[k][e], mxhw) * 448.0f : h[k][e] * f;
+      if (v < p.nvec)
+        stg_stream(static_cast<uint8_t*>(p.out) + t * H + v * 8,
+                   make_uint2(pack_e4m3x4(q[0], q[1], q[2], q[3]),
+                              pack_e4m3x4(q[4], q[5], q[6], q[7])));
+    }
+  } else {  // NVFP4: 16-element blocks = vectors (2m, 2m+1), held by lanes (c, c^1)
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int v = c + k * p.nthreads;
+      float y[8];
+      float amax = 0.0f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        y[e] = h[k][e] * rinv;
+        amax = fmaxf(amax, fabsf(y[e]));
+      }
+      amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+      const uint32_t sf = e4m3_code((amax * qc.gs) / 6.0f);
+      const float sfv = e4m3_value(sf);
+      const float mult = sfv == 0.0f ? 0.0f : qc.gs / sfv;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) y[e] *= mult;
+      if (v < p.nvec) {
+        stg_stream(static_cast<uint8_t*>(p.out) + t * (H / 2) + v * 4, pack_e2m1x8(y));
+        if ((v & 1) == 0) static_cast<uint8_t*>(p.out_scales)[t * (H / 16) + v / 2] =
+            static_cast<uint8_t>(sf);
+      }
+    }
+  }
+  return abort_all;
+}
+
+// This thread's weight and bias vectors (zero past the row).
+template <int kVec>
+__device__ __forceinline__ void load_row_constants(const Params& p, int c, uint4 (&w)[kVec],
+                                                   uint4 (&b)[kVec]) {
+#pragma unroll
+  for (int k = 0; k < kVec; ++k) {
+    const int v = c + k * p.nthreads;
+    const bool ok = v < p.nvec;
+    w[k] = ok ? ldg_keep(p.weight + v * 8) : make_uint4(0, 0, 0, 0);
+    b[k] = (ok && p.bias) ? ldg_keep(p.bias + v * 8) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+}  // namespace spk

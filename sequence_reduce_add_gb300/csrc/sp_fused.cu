@@ -1,0 +1,378 @@
+// sp_fused.cu — the C boundary (include/sp_fused.h): argument checks, launch selection and
+// kernel launches for the fused reduce + add + RMSNorm + quant stage on sm_103a.
+#include <cuda_runtime.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "sp_fused.h"
+#include "sp_kernels.cuh"
+
+namespace {
+
+constexpr int64_t kMaxHidden = 8 * 4 * spk::kMaxConsumerThreads;  // VEC 4 x 512 threads: 16384
+
+// ------------------------------------------------------------------------------ checks
+int64_t out_bytes_of(int64_t T_pad, int64_t H, int mode) {
+  switch (mode) {
+    case SP_QUANT_NONE: return T_pad * H * 2;
+    case SP_QUANT_FP8_STATIC:
+    case SP_QUANT_FP8_PER_TOKEN: return T_pad * H;
+    case SP_QUANT_NVFP4: return T_pad * (H / 2);
+    default: return -1;
+  }
+}
+
+int64_t scale_bytes_of(int64_t T_pad, int64_t H, int mode) {
+  switch (mode) {
+    case SP_QUANT_NONE:
+    case SP_QUANT_FP8_STATIC: return 0;
+    case SP_QUANT_FP8_PER_TOKEN: return T_pad * 4;
+    case SP_QUANT_NVFP4: return T_pad * (H / 16);
+    default: return -1;
+  }
+}
+
+bool overlaps(const void* p, int64_t pn, const void* q, int64_t qn) {
+  if (!p || !q || pn <= 0 || qn <= 0) return false;
+  const uintptr_t a = reinterpret_cast<uintptr_t>(p), b = reinterpret_cast<uintptr_t>(q);
+  return a < b + static_cast<uintptr_t>(qn) && b < a + static_cast<uintptr_t>(pn);
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The checks of sp_fused_reduce_norm, in the documented order. The shape rules restate the
+// shard checks of the PR #18671 notes (§5.2): the padded token count is a whole number of
+// equal shards, and the valid tokens fit in it.
+sp_status check(const void* partials, int tp, int64_t T_pad, int64_t T_valid, int64_t H,
+                const void* residual, const void* weight, const void* bias, float eps, int mode,
+                const float* scale, const void* out, const void* out_scales,
+                const void* residual_out) {
+  if (mode == SP_QUANT_FP8_DYNAMIC_PER_TENSOR) return SP_ERR_UNSUPPORTED;
+  if (mode < SP_QUANT_NONE || mode > SP_QUANT_NVFP4) return SP_ERR_INVALID_ARG;
+  if (tp < 1 || T_pad < 0 || T_valid < 0 || T_valid > T_pad) return SP_ERR_INVALID_ARG;
+  if (T_pad % tp != 0) return SP_ERR_INVALID_ARG;
+  if (H <= 0 || H % 8 != 0) return SP_ERR_INVALID_ARG;
+  if (mode == SP_QUANT_NVFP4 && H % 16 != 0) return SP_ERR_INVALID_ARG;
+  if (!(eps > 0.0f) || !std::isfinite(eps)) return SP_ERR_INVALID_ARG;
+  if (T_pad == 0) return SP_OK;
+  if (!partials || !weight || !out || !residual_out) return SP_ERR_INVALID_ARG;
+  if ((mode == SP_QUANT_FP8_STATIC || mode == SP_QUANT_NVFP4) && !scale) return SP_ERR_INVALID_ARG;
+  if ((mode == SP_QUANT_FP8_PER_TOKEN || mode == SP_QUANT_NVFP4) && !out_scales)
+    return SP_ERR_INVALID_ARG;
+  const int64_t rows = T_pad * H * 2;
+  const void* inputs[] = {partials, residual, weight, bias, scale};
+  const int64_t in_n[] = {rows * tp, rows, H * 2, H * 2, 4};
+  const void* outputs[] = {out, out_scales, residual_out};
+  const int64_t out_n[] = {out_bytes_of(T_pad, H, mode), scale_bytes_of(T_pad, H, mode), rows};
+  for (int o = 0; o < 3; ++o) {
+    for (int i = 0; i < 5; ++i) {
+      if (o == 2 && i == 1 && residual_out == residual) continue;  // in-place residual update
+      if (overlaps(outputs[o], out_n[o], inputs[i], in_n[i])) return SP_ERR_INVALID_ARG;
+    }
+    for (int q = o + 1; q < 3; ++q)
+      if (overlaps(outputs[o], out_n[o], outputs[q], out_n[q])) return SP_ERR_INVALID_ARG;
+  }
+  const void* all[] = {partials, residual, weight, bias, scale, out, out_scales, residual_out};
+  for (const void* ptr : all)
+    if (ptr && !aligned16(ptr)) return SP_ERR_ALIGNMENT;
+  if (H > kMaxHidden) return SP_ERR_UNSUPPORTED;
+  return SP_OK;
+}
+
+// ------------------------------------------------------------------------------ devices
+constexpr int kMaxDevices = 64;
+constexpr int kSmemPerSm = 233472;   // 228 KiB of shared memory per SM
+constexpr int kSmemPerCtaMax = 232448;  // 227 KiB opt-in limit per CTA
+constexpr int kSmemReservedPerCta = 1024;
+
+struct DeviceInfo {
+  int sms = 0;
+  std::atomic<bool> staged_attr_set[3][4] = {};
+};
+DeviceInfo g_devices[kMaxDevices];
+std::mutex g_devices_mutex;
+
+sp_status device_info(DeviceInfo** info) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SP_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_devices_mutex);
+  DeviceInfo& d = g_devices[dev];
+  if (d.sms == 0) {
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return SP_ERR_CUDA;
+    d.sms = sms;
+  }
+  *info = &d;
+  return SP_OK;
+}
+
+int vec_index(int vec) { return vec == 1 ? 0 : vec == 2 ? 1 : 2; }
+
+int consumer_threads(int64_t H, int vec) {
+  const int64_t nvec = H / 8;
+  const int64_t per = (nvec + vec - 1) / vec;
+  return static_cast<int>((per + 31) / 32 * 32);
+}
+
+// Dynamic shared memory of the staged kernel: [full barriers][empty barriers][reduction slots]
+// [abort flag] | weight copy [H] bf16, bias copy [H] bf16 | ring of `stages` segments.
+int wb_offset(int stages) {
+  const int head = stages * 16 + 64 * static_cast<int>(sizeof(spk::RedSlot)) + 16;
+  return (head + 127) / 128 * 128;
+}
+
+int ring_offset(int stages, int64_t H) {
+  return static_cast<int>((wb_offset(stages) + 4 * H + 127) / 128 * 128);
+}
+
+int seg_stride(int64_t H) { return static_cast<int>((H * 2 + 127) / 128 * 128); }
+
+int max_stages(int64_t H, int ctas_per_sm) {
+  int budget = kSmemPerSm / ctas_per_sm - kSmemReservedPerCta;
+  if (budget > kSmemPerCtaMax) budget = kSmemPerCtaMax;
+  const int stride = seg_stride(H);
+  int s = budget / stride;
+  while (s > 0 && ring_offset(s, H) + s * stride > budget) --s;
+  return s > 64 ? 64 : s;
+}
+
+// Grid of a persistent launch: SMs x CTAs per SM, where CTAs per SM is the requested number
+// capped at what the SM can hold for this kernel (registers, threads, shared memory), so the
+// grid is never a ragged second wave; and never more CTAs than rows.
+template <typename Kernel>
+cudaError_t persistent_grid(Kernel kernel, int threads, int smem, int ctas_per_sm,
+                            int64_t rows, const DeviceInfo* dev, int* grid) {
+  int resident = 0;
+  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (resident < 1) return cudaErrorInvalidConfiguration;
+  const int per_sm = ctas_per_sm < resident ? ctas_per_sm : resident;
+  int64_t g = static_cast<int64_t>(dev->sms) * per_sm;
+  if (g > rows) g = rows;
+  *grid = static_cast<int>(g);
+  return cudaSuccess;
+}
+
+template <int kVec, int kMode>
+cudaError_t launch_one(const sp_launch_config& cfg, const spk::Params& p, int smem,
+                       cudaStream_t stream, DeviceInfo* dev) {
+  int grid = 0;
+  if (cfg.kernel == SP_KERNEL_DIRECT) {
+    auto kernel = spk::k_direct<kVec, kMode>;
+    cudaError_t e = persistent_grid(kernel, p.nthreads, 0, cfg.ctas_per_sm, p.T_pad, dev, &grid);
+    if (e != cudaSuccess) return e;
+    kernel<<<grid, p.nthreads, 0, stream>>>(p);
+    return cudaGetLastError();
+  }
+  auto kernel = spk::k_staged<kVec, kMode>;
+  std::atomic<bool>& attr = dev->staged_attr_set[vec_index(kVec)][kMode];
+  if (!attr.load(std::memory_order_acquire)) {
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kSmemPerCtaMax);
+    if (e != cudaSuccess) return e;
+    attr.store(true, std::memory_order_release);
+  }
+  const int threads = p.nthreads + spk::kProducerThreads;
+  cudaError_t e = persistent_grid(kernel, threads, smem, cfg.ctas_per_sm, p.T_pad, dev, &grid);
+  if (e != cudaSuccess) return e;
+  kernel<<<grid, threads, smem, stream>>>(p);
+  return cudaGetLastError();
+}
+
+template <int kVec>
+cudaError_t launch_mode(int mode, const sp_launch_config& cfg, const spk::Params& p, int smem,
+                        cudaStream_t stream, DeviceInfo* dev) {
+  switch (mode) {
+    case SP_QUANT_NONE: return launch_one<kVec, spk::kModeNone>(cfg, p, smem, stream, dev);
+    case SP_QUANT_FP8_STATIC:
+      return launch_one<kVec, spk::kModeFp8Static>(cfg, p, smem, stream, dev);
+    case SP_QUANT_FP8_PER_TOKEN:
+      return launch_one<kVec, spk::kModeFp8PerToken>(cfg, p, smem, stream, dev);
+    default: return launch_one<kVec, spk::kModeNvfp4>(cfg, p, smem, stream, dev);
+  }
+}
+
+sp_status config_is_valid(const sp_launch_config& cfg, int64_t H) {
+  if (cfg.kernel != SP_KERNEL_STAGED && cfg.kernel != SP_KERNEL_DIRECT) return SP_ERR_INVALID_ARG;
+  if (cfg.vec_per_thread != 1 && cfg.vec_per_thread != 2 && cfg.vec_per_thread != 4)
+    return SP_ERR_INVALID_ARG;
+  if (cfg.ctas_per_sm < 1 || cfg.ctas_per_sm > 8) return SP_ERR_INVALID_ARG;
+  if (consumer_threads(H, cfg.vec_per_thread) > spk::kMaxConsumerThreads) return SP_ERR_UNSUPPORTED;
+  if (cfg.kernel == SP_KERNEL_STAGED) {
+    const int most = max_stages(H, cfg.ctas_per_sm);
+    if (cfg.stages < 0 || cfg.stages > most || most < 2 || cfg.stages == 1)
+      return SP_ERR_UNSUPPORTED;
+  }
+  return SP_OK;
+}
+
+sp_status run(const sp_launch_config& cfg_in, const void* partials, int tp, int64_t T_pad,
+              int64_t T_valid, int64_t H, const void* residual, const void* weight,
+              const void* bias, float eps, int mode, const float* scale, void* out,
+              void* out_scales, void* residual_out, cudaStream_t stream) {
+  sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, mode, scale,
+                       out, out_scales, residual_out);
+  if (st != SP_OK) return st;
+  st = config_is_valid(cfg_in, H);
+  if (st != SP_OK) return st;
+  if (T_pad == 0) return SP_OK;
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != SP_OK) return st;
+
+  sp_launch_config cfg = cfg_in;
+  spk::Params p{};
+  p.partials = static_cast<const uint16_t*>(partials);
+  p.residual = static_cast<const uint16_t*>(residual);
+  p.weight = static_cast<const uint16_t*>(weight);
+  p.bias = static_cast<const uint16_t*>(bias);
+  p.scale = scale;
+  p.out = out;
+  p.out_scales = out_scales;
+  p.residual_out = static_cast<uint16_t*>(residual_out);
+  p.T_pad = T_pad;
+  p.T_valid = T_valid;
+  p.plane = T_pad * H;
+  p.H = static_cast<int>(H);
+  p.nvec = static_cast<int>(H / 8);
+  p.tp = tp;
+  p.nthreads = consumer_threads(H, cfg.vec_per_thread);
+  p.eps = eps;
+  int smem = 0;
+  if (cfg.kernel == SP_KERNEL_STAGED) {
+    if (cfg.stages == 0) cfg.stages = max_stages(H, cfg.ctas_per_sm);
+    p.stages = cfg.stages;
+    p.seg_stride = seg_stride(H);
+    p.wb_offset = wb_offset(cfg.stages);
+    p.ring_offset = ring_offset(cfg.stages, H);
+    smem = p.ring_offset + p.stages * p.seg_stride;
+  }
+  cudaError_t e;
+  switch (cfg.vec_per_thread) {
+    case 1: e = launch_mode<1>(mode, cfg, p, smem, stream, dev); break;
+    case 2: e = launch_mode<2>(mode, cfg, p, smem, stream, dev); break;
+    default: e = launch_mode<4>(mode, cfg, p, smem, stream, dev); break;
+  }
+  return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
+                           sp_launch_config* config) {
+  (void)tp;
+  (void)T_pad;
+  if (!config || H <= 0 || H % 8 != 0) return SP_ERR_INVALID_ARG;
+  if (quant_mode < SP_QUANT_NONE || quant_mode > SP_QUANT_FP8_DYNAMIC_PER_TENSOR)
+    return SP_ERR_INVALID_ARG;
+  if (H > kMaxHidden) return SP_ERR_UNSUPPORTED;
+  // Staged kernel, two 16-byte vectors per consumer thread (four beyond H = 8192), a ring of
+  // 3-4 row segments per CTA and as many CTAs per SM (up to 4) as the SM holds: about
+  // 100-130 KB of reads in flight per SM, which measured best on GB300 for H = 4096-8192.
+  sp_launch_config c{};
+  c.kernel = SP_KERNEL_STAGED;
+  c.vec_per_thread = 2;
+  if (consumer_threads(H, c.vec_per_thread) > spk::kMaxConsumerThreads) c.vec_per_thread = 4;
+  c.stages = H <= 5120 ? 3 : 4;
+  c.ctas_per_sm = 4;
+  while (c.ctas_per_sm > 1 && max_stages(H, c.ctas_per_sm) < c.stages) --c.ctas_per_sm;
+  if (max_stages(H, c.ctas_per_sm) < c.stages) c.stages = max_stages(H, c.ctas_per_sm);
+  if (c.stages < 2) {
+    c.kernel = SP_KERNEL_DIRECT;
+    c.stages = 0;
+  }
+  *config = c;
+  return SP_OK;
+}
+
+sp_status sp_fused_reduce_norm(const void* partials, int tp, int64_t T_pad, int64_t T_valid,
+                               int64_t H, const void* residual, const void* weight,
+                               const void* bias, float eps, int quant_mode, const float* scale,
+                               void* out, void* out_scales, void* residual_out,
+                               sp_stream_t stream) {
+  sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode,
+                       scale, out, out_scales, residual_out);
+  if (st != SP_OK) return st;
+  sp_launch_config cfg;
+  st = sp_select_launch(tp, T_pad, H, quant_mode, &cfg);
+  if (st != SP_OK) return st;
+  return run(cfg, partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode, scale,
+             out, out_scales, residual_out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sp_status sp_fused_reduce_norm_with_config(const sp_launch_config* config, const void* partials,
+                                           int tp, int64_t T_pad, int64_t T_valid, int64_t H,
+                                           const void* residual, const void* weight,
+                                           const void* bias, float eps, int quant_mode,
+                                           const float* scale, void* out, void* out_scales,
+                                           void* residual_out, sp_stream_t stream) {
+  if (!config) return SP_ERR_INVALID_ARG;
+  return run(*config, partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode,
+             scale, out, out_scales, residual_out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+sp_status sp_check_args(const void* partials, int tp, int64_t T_pad, int64_t T_valid, int64_t H,
+                        const void* residual, const void* weight, const void* bias, float eps,
+                        int quant_mode, const float* scale, const void* out,
+                        const void* out_scales, const void* residual_out) {
+  return check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode, scale,
+               out, out_scales, residual_out);
+}
+
+int64_t sp_pad_tokens(int64_t T, int tp) {
+  if (T < 0 || tp < 1) return -1;
+  return (T + tp - 1) / tp * tp;
+}
+
+sp_status sp_shard_rows(int64_t T_pad, int tp, int rank, int64_t* start, int64_t* len) {
+  if (!start || !len || tp < 1 || T_pad < 0 || T_pad % tp != 0 || rank < 0 || rank >= tp)
+    return SP_ERR_INVALID_ARG;
+  const int64_t s = T_pad / tp;
+  *start = static_cast<int64_t>(rank) * s;
+  *len = s;
+  return SP_OK;
+}
+
+int64_t sp_out_bytes(int64_t T_pad, int64_t H, int quant_mode) {
+  if (T_pad < 0 || H < 0) return -1;
+  return out_bytes_of(T_pad, H, quant_mode);
+}
+
+int64_t sp_out_scales_bytes(int64_t T_pad, int64_t H, int quant_mode) {
+  if (T_pad < 0 || H < 0) return -1;
+  return scale_bytes_of(T_pad, H, quant_mode);
+}
+
+int64_t sp_max_hidden(void) { return kMaxHidden; }
+
+const char* sp_status_string(int status) {
+  switch (status) {
+    case SP_OK: return "SP_OK";
+    case SP_ERR_INVALID_ARG: return "SP_ERR_INVALID_ARG";
+    case SP_ERR_UNSUPPORTED: return "SP_ERR_UNSUPPORTED";
+    case SP_ERR_ALIGNMENT: return "SP_ERR_ALIGNMENT";
+    case SP_ERR_CUDA: return "SP_ERR_CUDA";
+    default: return "SP_UNKNOWN_STATUS";
+  }
+}
+
+sp_status sp_device_error(uint32_t* flags, int clear) {
+  if (!flags) return SP_ERR_INVALID_ARG;
+  unsigned int v = 0;
+  if (cudaMemcpyFromSymbol(&v, spk::g_error_flags, sizeof(v)) != cudaSuccess) return SP_ERR_CUDA;
+  if (clear) {
+    const unsigned int zero = 0;
+    if (cudaMemcpyToSymbol(spk::g_error_flags, &zero, sizeof(zero)) != cudaSuccess)
+      return SP_ERR_CUDA;
+  }
+  *flags = v;
+  return SP_OK;
+}
+
+}  // extern "C"

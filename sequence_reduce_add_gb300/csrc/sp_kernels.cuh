@@ -1,0 +1,222 @@
+// sp_kernels.cuh — the two kernels of the fused stage. Both map one token row at a time to one
+// CTA (rows are independent: RMSNorm and every scale kind used here are per token), walk rows
+// with a grid stride in token order, and make a single pass over HBM: every partial, residual
+// and output byte of a valid row is read or written exactly once; padding rows are written as
+// zeros without any read.
+//
+// Thread c of the CTA's consumer threads owns 16-byte vectors v = c + k*nthreads (k < VEC) of
+// the row, i.e. 8*VEC columns, held as fp32 accumulators in registers for the whole row.
+//
+//   k_staged  A producer thread streams the row's tp partial rows and its residual row (each a
+//             contiguous 2*H-byte segment) into a ring of shared-memory stages with bulk
+//             asynchronous copies (cp.async.bulk, completion on an mbarrier per stage) while the
+//             consumer warps add the segments that have landed. The ring runs ahead across rows,
+//             so HBM stays busy through each row's reduction and epilogue, and the bytes in flight
+//             per SM are set by the ring depth rather than by registers.
+//   k_direct  The consumer threads load their vectors of every segment straight into registers
+//             with 128-bit non-coherent loads, four partials at a time.
+#pragma once
+
+#include "sp_device.cuh"
+
+namespace spk {
+
+constexpr int kMaxConsumerThreads = 512;  // 16 warps
+constexpr int kProducerThreads = 32;
+
+// ----------------------------------------------------------------------------------- staged
+template <int kVec, int kMode>
+__global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
+    k_staged(const Params p) {
+  extern __shared__ __align__(128) unsigned char smem[];
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem);
+  uint64_t* empty = full + p.stages;
+  RedSlot* slots = reinterpret_cast<RedSlot*>(empty + p.stages);
+  int* abort_flag = reinterpret_cast<int*>(slots + 64);
+  unsigned char* ring = smem + p.ring_offset;
+
+  const int tid = threadIdx.x;
+  const int nc = p.nthreads;
+  const int nseg = p.tp + (p.residual ? 1 : 0);
+  const uint32_t seg_bytes = static_cast<uint32_t>(p.H) * 2u;
+  const int64_t H = p.H;
+
+  if (tid == 0) {
+    for (int s = 0; s < p.stages; ++s) {
+      mbar_init(smem_addr(full + s), 1);
+      mbar_init(smem_addr(empty + s), static_cast<uint32_t>(nc >> 5));
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (tid >= nc) {
+    // ------------------------------------------------------------ producer (one thread)
+    if (tid != nc) return;
+    const uint64_t policy = l2_evict_first_policy();
+    int stage = 0;
+    uint32_t phase = 0;
+    int64_t issued = 0;
+    bool aborted = false;
+    for (int64_t t = blockIdx.x; t < p.T_valid && !aborted; t += gridDim.x) {
+      for (int seg = 0; seg < nseg; ++seg) {
+        const uint16_t* src = seg < p.tp ? p.partials + seg * p.plane + t * H : p.residual + t * H;
+        if (!mbar_wait_bounded(smem_addr(empty + stage), phase ^ 1u, abort_flag)) {
+          if (!*static_cast<volatile int*>(abort_flag)) atomicOr(&g_error_flags, kErrWaitTimeout);
+          *static_cast<volatile int*>(abort_flag) = 1;
+          aborted = true;
+          break;
+        }
+        const uint32_t bar = smem_addr(full + stage);
+        mbar_arrive_expect_tx(bar, seg_bytes);
+        bulk_g2s(smem_addr(ring + stage * p.seg_stride), src, seg_bytes, bar, policy);
+        ++issued;
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+      }
+    }
+    // Let every copy still in flight land before this CTA can exit: wait for the last issued
+    // phase of each stage.
+    const int64_t used = issued < p.stages ? issued : p.stages;
+    for (int64_t s = 0; s < used; ++s) {
+      const int64_t last = issued - 1 - ((issued - 1 - s) % p.stages);  // last issue on stage s
+      const uint32_t par = static_cast<uint32_t>((last / p.stages) & 1);
+      if (!mbar_wait_bounded(smem_addr(full + s), par, nullptr))
+        atomicOr(&g_error_flags, kErrWaitTimeout);
+    }
+    return;
+  }
+
+  // -------------------------------------------------------------- consumers
+  const int c = tid;
+  const int lane = tid & 31;
+  // This thread's weight and bias vectors live in shared memory (read once per row) rather than
+  // in registers, so that more rows fit on an SM. Each thread writes and reads only its own
+  // vectors, so no barrier is needed.
+  uint4* wb = reinterpret_cast<uint4*>(smem + p.wb_offset);
+  {
+    uint4 w0[kVec], b0[kVec];
+    load_row_constants<kVec>(p, c, w0, b0);
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int v = c + k * nc;
+      if (v < p.nvec) {
+        wb[v] = w0[k];
+        wb[p.nvec + v] = b0[k];
+      }
+    }
+  }
+  const QuantConst qc = load_quant_const<kMode>(p);
+
+  int stage = 0;
+  uint32_t phase = 0;
+  int parity = 0;
+  for (int64_t t = blockIdx.x; t < p.T_pad; t += gridDim.x) {
+    if (t >= p.T_valid) {
+      zero_row<kVec, kMode>(p, t, c);
+      continue;
+    }
+    float h[kVec][8];
+#pragma unroll
+    for (int k = 0; k < kVec; ++k)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) h[k][e] = 0.0f;
+
+    int aborted = 0;
+    for (int seg = 0; seg < nseg; ++seg) {
+      if (!aborted && !mbar_wait_bounded(smem_addr(full + stage), phase, abort_flag)) {
+        if (!*static_cast<volatile int*>(abort_flag)) atomicOr(&g_error_flags, kErrWaitTimeout);
+        *static_cast<volatile int*>(abort_flag) = 1;
+        aborted = 1;
+      }
+      const unsigned char* src = ring + stage * p.seg_stride;
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) {
+        const int v = c + k * nc;
+        if (v < p.nvec) add_bf16x8(*reinterpret_cast<const uint4*>(src + v * 16), h[k]);
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(smem_addr(empty + stage));
+      if (++stage == p.stages) {
+        stage = 0;
+        phase ^= 1u;
+      }
+    }
+    uint4 w[kVec];
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int v = c + k * nc;
+      const bool ok = v < p.nvec;
+      if (ok) add_bf16x8(wb[p.nvec + v], h[k]);
+      w[k] = ok ? wb[v] : make_uint4(0, 0, 0, 0);
+    }
+    const int stop = finish_row<kVec, kMode>(p, t, h, w, qc, slots, parity, c, aborted);
+    parity ^= 1;
+    if (stop) break;  // every consumer sees the same vote, so all leave together
+  }
+}
+
+// ----------------------------------------------------------------------------------- direct
+template <int kVec, int kMode>
+__global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) {
+  __shared__ RedSlot slots[64];
+  const int c = threadIdx.x;
+  const int nc = p.nthreads;
+  const int64_t H = p.H;
+  uint4 w[kVec], b[kVec];
+  load_row_constants<kVec>(p, c, w, b);
+  const QuantConst qc = load_quant_const<kMode>(p);
+
+  int parity = 0;
+  for (int64_t t = blockIdx.x; t < p.T_pad; t += gridDim.x) {
+    if (t >= p.T_valid) {
+      zero_row<kVec, kMode>(p, t, c);
+      continue;
+    }
+    float h[kVec][8];
+#pragma unroll
+    for (int k = 0; k < kVec; ++k)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) h[k][e] = 0.0f;
+
+    const uint16_t* row = p.partials + t * H;
+    int r = 0;
+    for (; r + 4 <= p.tp; r += 4) {
+      uint4 x[4][kVec];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) {
+          const int v = c + k * nc;
+          x[u][k] = v < p.nvec ? ldg_stream(row + (r + u) * p.plane + v * 8) : make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int k = 0; k < kVec; ++k) add_bf16x8(x[u][k], h[k]);
+    }
+    for (; r < p.tp; ++r) {
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) {
+        const int v = c + k * nc;
+        if (v < p.nvec) add_bf16x8(ldg_stream(row + r * p.plane + v * 8), h[k]);
+      }
+    }
+    if (p.residual) {
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) {
+        const int v = c + k * nc;
+        if (v < p.nvec) add_bf16x8(ldg_stream(p.residual + t * H + v * 8), h[k]);
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) add_bf16x8(b[k], h[k]);
+    finish_row<kVec, kMode>(p, t, h, w, qc, slots, parity, c, 0);
+    parity ^= 1;
+  }
+}
+
+}  // namespace spk

@@ -1,0 +1,170 @@
+"""The C boundary without a GPU: the library loads, exports every function include/*.h declares,
+its host-only helpers follow the pages' layout rules, and its argument checks return the same
+statuses as the oracle's rules. Nothing here launches a kernel or touches device memory."""
+import ctypes
+import glob
+import json
+import os
+import re
+
+import pytest
+
+import oracle
+import sequence_reduce_add_gb300 as sp
+from sequence_reduce_add_gb300 import build as sp_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sp_build.build()
+    return sp.load_library()
+
+
+def declared_functions() -> list[str]:
+    names = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        names += re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(sp_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("sp_fused_reduce_norm", "sp_check_args", "sp_pad_tokens", "sp_shard_rows",
+                     "sp_status_string", "sp_device_error"):
+        assert required in names
+
+
+def test_library_exports_every_declared_function(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    assert [sp.sp_status_string(s) for s in range(5)] == [
+        "SP_OK", "SP_ERR_INVALID_ARG", "SP_ERR_UNSUPPORTED", "SP_ERR_ALIGNMENT", "SP_ERR_CUDA"]
+    assert sp.sp_status_string(99) == "SP_UNKNOWN_STATUS"
+
+
+def test_padding_and_shards_match_the_pr_example(lib):
+    with open(os.path.join(ROOT, "tests", "golden", "shard_layout_tp16_t3500.json")) as f:
+        gold = json.load(f)
+    tp = gold["tp"]
+    assert sp.sp_pad_tokens(gold["num_tokens"], tp) == gold["num_tokens_pad"]
+    for r in range(tp):
+        assert sp.sp_shard_rows(gold["num_tokens_pad"], tp, r) == (gold["shard_starts"][r],
+                                                                    gold["local_tokens"])
+    assert sp.sp_pad_tokens(4093, 4) == 4096 and sp.sp_pad_tokens(0, 4) == 0
+    assert sp.sp_pad_tokens(8192, 8) == 8192 and sp.sp_pad_tokens(7, 1) == 7
+    assert sp.sp_pad_tokens(-1, 4) == -1 and sp.sp_pad_tokens(5, 0) == -1
+    with pytest.raises(sp.SpError):
+        sp.sp_shard_rows(3500, 16, 0)
+    with pytest.raises(sp.SpError):
+        sp.sp_shard_rows(3504, 16, 16)
+
+
+def test_output_sizes(lib):
+    assert sp.sp_out_bytes(4096, 4096, "none") == 4096 * 4096 * 2
+    assert sp.sp_out_bytes(8192, 7168, "fp8_static") == 8192 * 7168
+    assert sp.sp_out_bytes(16384, 5120, "nvfp4") == 16384 * 2560
+    assert sp.sp_out_scales_bytes(3504, 8192, "fp8_per_token") == 3504 * 4
+    assert sp.sp_out_scales_bytes(16384, 5120, "nvfp4") == 16384 * 320
+    assert sp.sp_out_scales_bytes(10, 64, "none") == 0
+    assert sp.sp_out_bytes(10, 64, 9) == -1
+    assert sp.sp_max_hidden() >= 8192
+
+
+def test_launch_selection(lib):
+    for tp, T, H in ((2, 64, 1024), (4, 4096, 4096), (8, 8192, 7168), (16, 3504, 8192),
+                     (8, 16384, 5120), (1, 8, 16384), (3, 9, 8)):
+        cfg = sp.sp_select_launch(tp, T, H, "none")
+        assert cfg.kernel in (0, 1) and cfg.vec_per_thread in (1, 2, 4)
+        assert cfg.ctas_per_sm >= 1
+    with pytest.raises(sp.SpError):
+        sp.sp_select_launch(2, 8, sp.sp_max_hidden() + 8, "none")
+
+
+A = 1 << 20  # fake 16-byte-aligned addresses: compared, never dereferenced
+
+
+def _base():
+    return dict(partials=A, tp=4, T_pad=16, T_valid=13, H=64, residual=A * 8, weight=A * 9,
+                bias=A * 10, eps=1e-6, quant_mode="fp8_per_token", scale=None, out=A * 11,
+                out_scales=A * 12, residual_out=A * 13)
+
+
+CASES = [
+    ({}, "SP_OK"),
+    ({"quant_mode": "fp8_dynamic_per_tensor"}, "SP_ERR_UNSUPPORTED"),
+    ({"quant_mode": 7}, "SP_ERR_INVALID_ARG"),
+    ({"quant_mode": -1}, "SP_ERR_INVALID_ARG"),
+    ({"tp": 0}, "SP_ERR_INVALID_ARG"),
+    ({"T_pad": 18}, "SP_ERR_INVALID_ARG"),
+    ({"T_pad": -4}, "SP_ERR_INVALID_ARG"),
+    ({"T_valid": 17}, "SP_ERR_INVALID_ARG"),
+    ({"T_valid": -1}, "SP_ERR_INVALID_ARG"),
+    ({"H": 60}, "SP_ERR_INVALID_ARG"),
+    ({"H": 0}, "SP_ERR_INVALID_ARG"),
+    ({"H": 72, "quant_mode": "nvfp4", "scale": A * 14}, "SP_ERR_INVALID_ARG"),
+    ({"eps": 0.0}, "SP_ERR_INVALID_ARG"),
+    ({"eps": -1e-6}, "SP_ERR_INVALID_ARG"),
+    ({"eps": float("nan")}, "SP_ERR_INVALID_ARG"),
+    ({"partials": None}, "SP_ERR_INVALID_ARG"),
+    ({"weight": None}, "SP_ERR_INVALID_ARG"),
+    ({"out": None}, "SP_ERR_INVALID_ARG"),
+    ({"residual_out": None}, "SP_ERR_INVALID_ARG"),
+    ({"out_scales": None}, "SP_ERR_INVALID_ARG"),
+    ({"quant_mode": "fp8_static", "out_scales": None}, "SP_ERR_INVALID_ARG"),  # no scale
+    ({"quant_mode": "nvfp4", "scale": None}, "SP_ERR_INVALID_ARG"),
+    ({"residual": None}, "SP_OK"),
+    ({"bias": None}, "SP_OK"),
+    ({"residual_out": A * 8}, "SP_OK"),
+    ({"residual_out": A * 8 + 16}, "SP_ERR_INVALID_ARG"),
+    ({"out": A + 64}, "SP_ERR_INVALID_ARG"),
+    ({"out": A * 13 + 32}, "SP_ERR_INVALID_ARG"),
+    ({"out_scales": A * 11 + 16}, "SP_ERR_INVALID_ARG"),
+    ({"T_pad": 0, "T_valid": 0, "partials": None, "out": None}, "SP_OK"),
+    ({"partials": A + 8}, "SP_ERR_ALIGNMENT"),
+    ({"out": A * 11 + 4}, "SP_ERR_ALIGNMENT"),
+    ({"residual": A * 8 + 2, "residual_out": A * 13}, "SP_ERR_ALIGNMENT"),
+    ({"H": 1 << 16}, "SP_ERR_UNSUPPORTED"),
+]
+
+
+@pytest.mark.parametrize("kw,want", CASES)
+def test_argument_checks(lib, kw, want):
+    a = {**_base(), **kw}
+    st = sp.sp_check_args(**a)
+    assert sp.sp_status_string(st) == want
+    # the oracle applies the same shape, mode and pointer rules (alignment and the largest H
+    # are device-path limits, and the oracle reads the scale value, so those cases are skipped)
+    if want not in ("SP_ERR_ALIGNMENT",) and not (kw.get("H", 0) > 16384) and "scale" not in kw:
+        ost = oracle.check_args(a["partials"], a["tp"], a["T_pad"], a["T_valid"], a["H"],
+                                a["residual"], a["weight"], a["bias"], a["eps"],
+                                sp._mode(a["quant_mode"]), None, a["out"], a["out_scales"],
+                                a["residual_out"])
+        assert ost == st
+
+
+def test_main_entry_rejects_before_any_cuda_call(lib):
+    # invalid arguments: the status comes back from the checks, no CUDA call is made
+    a = _base()
+    f = lib.sp_fused_reduce_norm
+    st = f(a["partials"], 4, 18, 13, 64, a["residual"], a["weight"], a["bias"], ctypes.c_float(1e-6),
+           2, None, a["out"], a["out_scales"], a["residual_out"], None)
+    assert sp.sp_status_string(st) == "SP_ERR_INVALID_ARG"
+    st = f(a["partials"], 4, 16, 13, 64, a["residual"], a["weight"], a["bias"], ctypes.c_float(1e-6),
+           4, None, a["out"], a["out_scales"], a["residual_out"], None)
+    assert sp.sp_status_string(st) == "SP_ERR_UNSUPPORTED"
+
+
+def test_product_path_does_not_reference_the_oracle():
+    pkg = os.path.join(ROOT, "sequence_reduce_add_gb300")
+    for path in glob.glob(os.path.join(pkg, "**", "*"), recursive=True):
+        if os.path.isfile(path) and path.endswith((".py", ".cu", ".cuh", ".h")):
+            src = open(path).read()
+            assert "import oracle" not in src and "from oracle" not in src, path
+            assert "sp_oracle" not in src and "libsporacle" not in src, path
