@@ -273,16 +273,22 @@ class OracleRunner:
 
 
 def cpu_baseline(w: dict, host_in: dict, target_s: float = 12.0) -> dict:
-    """The oracle as it stands, on a bounded row sample of the workload, on all host cores."""
+    """The oracle as it stands, on all host cores, over a bounded sample of about `target_s`
+    seconds: consecutive valid rows of the workload, wrapping around when the sample is larger
+    than the workload."""
     runner = OracleRunner(w, host_in)
-    n = runner.rows_for(target_s)
+    want = runner.rows_for(target_s)
     runner.next_row = 0
-    t, nbytes = runner.run(n)
-    n = min(n, w["T_valid"])
-    return {"value": nbytes / t / 1e9, "unit": "GB/s", "cores": runner.cores, "kind": "oracle",
-            "sample": f"rows 0..{n - 1} of {w['T_valid']} valid rows "
-                      f"({nbytes / 1e6:.1f} MB algorithmic), {runner.cores} threads, {t:.1f} s",
-            "mtokens_per_s": n / t / 1e6}
+    done, secs, nbytes = 0, 0.0, 0
+    while done < want:
+        n = min(w["T_valid"], want - done)
+        dt, b = runner.run(n)
+        done, secs, nbytes = done + n, secs + dt, nbytes + b
+    return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": runner.cores, "kind": "oracle",
+            "sample": f"{done} valid rows ({done / w['T_valid']:.2f} passes over the workload's "
+                      f"{w['T_valid']} rows, {nbytes / 1e6:.0f} MB algorithmic), "
+                      f"{runner.cores} threads, {secs:.1f} s",
+            "mtokens_per_s": done / secs / 1e6}
 
 
 def run_ours(args) -> None:
@@ -323,7 +329,7 @@ def run_ours(args) -> None:
     torch.cuda.synchronize()
     with ClockSampler(local) as clocks:
         t0 = time.time()
-        total_ms, launch_ms = time_kernel_loop(lib, problems, args.steps, stream, True)
+        total_ms, _ = time_kernel_loop(lib, problems, args.steps, stream, False)
         t1 = time.time()
     torch.cuda.synchronize()
     if dist:
@@ -334,7 +340,13 @@ def run_ours(args) -> None:
     ms_per_step = total_ms / args.steps
     value = one * args.steps * world / (total_ms / 1e3) / 1e9
     mtok = w["T_valid"] * args.steps * world / (total_ms / 1e3) / 1e6
-    kernel_ms = float(np.mean(launch_ms))
+    # The timed loop is one kernel per step launched back to back (consecutive launches overlap
+    # their launch latency and prologue through programmatic dependent launch), so the kernel's
+    # average launch duration is the timed region over the launches. An event-bracketed launch
+    # (no overlap with its neighbours) is reported beside it.
+    kernel_ms = ms_per_step
+    _, isolated = time_kernel_loop(lib, problems, min(args.steps, 300), stream, True)
+    isolated_ms = float(np.mean(isolated))
     peak, peak_kind = measured_peak()
     achieved = one / (kernel_ms / 1e3) / 1e9
 
@@ -371,6 +383,8 @@ def run_ours(args) -> None:
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": ncu_traffic(w["name"]), "kernel_ms": round(kernel_ms, 6),
+                     "isolated_launch_ms": round(isolated_ms, 6),
+                     "isolated_frac": round(one / (isolated_ms / 1e3) / 1e9 / peak, 4),
                      "kernel": "k_staged" if cfg["kernel"] == 0 else "k_direct"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
@@ -394,16 +408,45 @@ def bench_extra(lib, sp, synth, w, device, stream, peak) -> dict:
     steps = max(20, int(0.25e9 / max(one, 1)) * 4)
     steps = min(steps, 4000)
     time_kernel_loop(lib, problems, 10, stream, False)
-    total, launches = time_kernel_loop(lib, problems, steps, stream, True)
-    k = float(np.mean(launches))
+    total, _ = time_kernel_loop(lib, problems, steps, stream, False)
+    _, launches = time_kernel_loop(lib, problems, min(steps, 100), stream, True)
+    k = total / steps
     gbs = one / (k / 1e3) / 1e9
     res = {"GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
            "mtokens_per_s": round(w["T_valid"] / (k / 1e3) / 1e6, 3), "kernel_us": round(k * 1e3, 2),
-           "step_us": round(total / steps * 1e3, 2), "steps": steps, "bytes": one,
+           "isolated_launch_us": round(float(np.mean(launches)) * 1e3, 2), "steps": steps,
+           "bytes": one,
            "sets": len(problems)}
     del problems
     torch.cuda.empty_cache()
     return res
+
+
+def run_kernel_only(args) -> None:
+    """Warm-up and timed launches of the workload's kernel only, rotating over resident sets;
+    prints a short JSON line (the launch sequence that profiler captures are taken from)."""
+    import sequence_reduce_add_gb300 as sp
+    from sequence_reduce_add_gb300 import build as sp_build
+    from sequence_reduce_add_gb300 import synth
+    sp_build.build()
+    lib = sp.load_library()
+    device = torch.device("cuda", 0)
+    w = synth.workload(args.workload if not str(args.workload).isdigit() else int(args.workload))
+    base = Problem(w, synth.BASE_SEED + 1 + synth.WORKLOADS.index(
+        next(x for x in synth.WORKLOADS if x["name"] == w["name"])), device, sp)
+    sets = max(2, min(8, -(-(4 * L2_BYTES) // base.nbytes())))
+    problems = [base] + [Problem(w, base.inp["seed"] + 1000 * k, device, sp)
+                         for k in range(1, sets)]
+    stream = torch.cuda.Stream(device=device)
+    if args.warmup:
+        time_kernel_loop(lib, problems, args.warmup, stream, False)
+    total_ms, launches = time_kernel_loop(lib, problems, args.steps, stream, True)
+    one = algorithmic_bytes(w["tp"], w["T_valid"], w["T_pad"], w["H"], w["mode"])
+    k = float(np.mean(launches))
+    print(json.dumps({"workload": w["name"], "launches": args.steps, "sets": len(problems),
+                      "kernel_us": round(k * 1e3, 2), "GB_per_s": round(one / k / 1e6, 1),
+                      "launch": sp.sp_select_launch(w["tp"], w["T_pad"], w["H"],
+                                                    w["mode"]).as_dict()}), flush=True)
 
 
 # ------------------------------------------------------------------------------ reference arm
@@ -463,11 +506,15 @@ def main() -> None:
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-extras", action="store_true")
+    ap.add_argument("--kernel-only", action="store_true",
+                    help="only warm-up + timed kernel launches of the workload (for profilers)")
     ap.add_argument("--reference-budget-s", type=float, default=60.0,
                     help="CPU seconds for the whole reference-arm run (bounded row samples)")
     args = ap.parse_args()
     if args.impl == "reference":
         run_reference(args)
+    elif args.kernel_only:
+        run_kernel_only(args)
     else:
         run_ours(args)
 

@@ -225,6 +225,7 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
                                                   const volatile int* abort) {
   if (mbar_try_wait(bar, parity)) return true;
+  if (mbar_try_wait_sleep(bar, parity, kWaitSleepHintNs)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, kWaitSleepHintNs)) return true;
@@ -248,6 +249,23 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void* src, uint32_t
       "[%0], [%1], %2, [%3], %4;" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar), "l"(policy)
       : "memory");
+}
+
+// Prefetch `bytes` at `src` into L2 (no shared memory, no completion). Changes no memory, so it
+// may run before griddepcontrol.wait: L2 is where every write becomes visible, so a line
+// prefetched early can never be stale.
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
+// Programmatic dependent launch: let the next kernel of the stream be scheduled once every CTA
+// of this grid got here; and block until the previous kernel of the stream has completed and
+// its writes are visible (a no-op when the launch has no programmatic dependency).
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait_prerequisites() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {

@@ -157,6 +157,24 @@ cudaError_t persistent_grid(Kernel kernel, int threads, int smem, int ctas_per_s
   return cudaSuccess;
 }
 
+// Launch with programmatic stream serialisation: the kernel may be scheduled while the previous
+// kernel of the stream finishes; it waits (griddepcontrol.wait) before touching global memory.
+template <typename Kernel>
+cudaError_t launch_pdl(Kernel kernel, int grid, int threads, int smem, cudaStream_t stream,
+                       const spk::Params& p) {
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(static_cast<unsigned>(grid));
+  lc.blockDim = dim3(static_cast<unsigned>(threads));
+  lc.dynamicSmemBytes = static_cast<size_t>(smem);
+  lc.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  return cudaLaunchKernelEx(&lc, kernel, p);
+}
+
 template <int kVec, int kMode>
 cudaError_t launch_one(const sp_launch_config& cfg, const spk::Params& p, int smem,
                        cudaStream_t stream, DeviceInfo* dev) {
@@ -165,8 +183,8 @@ cudaError_t launch_one(const sp_launch_config& cfg, const spk::Params& p, int sm
     auto kernel = spk::k_direct<kVec, kMode>;
     cudaError_t e = persistent_grid(kernel, p.nthreads, 0, cfg.ctas_per_sm, p.T_pad, dev, &grid);
     if (e != cudaSuccess) return e;
-    kernel<<<grid, p.nthreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    e = launch_pdl(kernel, grid, p.nthreads, 0, stream, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
   }
   auto kernel = spk::k_staged<kVec, kMode>;
   std::atomic<bool>& attr = dev->staged_attr_set[vec_index(kVec)][kMode];
@@ -179,8 +197,8 @@ cudaError_t launch_one(const sp_launch_config& cfg, const spk::Params& p, int sm
   const int threads = p.nthreads + spk::kProducerThreads;
   cudaError_t e = persistent_grid(kernel, threads, smem, cfg.ctas_per_sm, p.T_pad, dev, &grid);
   if (e != cudaSuccess) return e;
-  kernel<<<grid, threads, smem, stream>>>(p);
-  return cudaGetLastError();
+  e = launch_pdl(kernel, grid, threads, smem, stream, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int kVec>

@@ -48,7 +48,17 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
     }
     *abort_flag = 0;
     fence_mbar_init();
+  } else if (tid == nc) {
+    // While the previous kernel of the stream may still be running, pull this CTA's first ring
+    // of segments into L2 so that the first bulk copies after the wait hit L2.
+    int n = 0;
+    for (int64_t t = blockIdx.x; t < p.T_valid && n < p.stages; t += gridDim.x)
+      for (int seg = 0; seg < nseg && n < p.stages; ++seg, ++n)
+        bulk_prefetch_l2(seg < p.tp ? p.partials + seg * p.plane + t * H : p.residual + t * H,
+                         seg_bytes);
   }
+  pdl_launch_dependents();
+  pdl_wait_prerequisites();
   __syncthreads();
 
   if (tid >= nc) {
@@ -166,6 +176,8 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
   const int c = threadIdx.x;
   const int nc = p.nthreads;
   const int64_t H = p.H;
+  pdl_launch_dependents();
+  pdl_wait_prerequisites();
   uint4 w[kVec], b[kVec];
   load_row_constants<kVec>(p, c, w, b);
   const QuantConst qc = load_quant_const<kMode>(p);
