@@ -291,6 +291,23 @@ def cpu_baseline(w: dict, host_in: dict, target_s: float = 12.0) -> dict:
             "mtokens_per_s": done / secs / 1e6}
 
 
+def max_over_ranks(value: float, device) -> float:
+    """The largest `value` over the ranks of the default process group (the slowest rank's
+    time); the value itself when no group is initialised."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_throughput(bytes_per_step: int, steps: int, world: int, max_ms: float) -> float:
+    """GB/s over all ranks: every rank moves bytes_per_step per step (independent replicas),
+    divided by the slowest rank's timed region."""
+    return bytes_per_step * steps * world / (max_ms / 1e3) / 1e9
+
+
 def run_ours(args) -> None:
     import sequence_reduce_add_gb300 as sp
     from sequence_reduce_add_gb300 import build as sp_build
@@ -334,11 +351,9 @@ def run_ours(args) -> None:
     torch.cuda.synchronize()
     if dist:
         dist.barrier()
-        t = torch.tensor([total_ms], device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+        total_ms = max_over_ranks(total_ms, device)
     ms_per_step = total_ms / args.steps
-    value = one * args.steps * world / (total_ms / 1e3) / 1e9
+    value = whole_job_throughput(one, args.steps, world, total_ms)
     mtok = w["T_valid"] * args.steps * world / (total_ms / 1e3) / 1e6
     # The timed loop is one kernel per step launched back to back (consecutive launches overlap
     # their launch latency and prologue through programmatic dependent launch), so the kernel's
