@@ -127,6 +127,22 @@ sp_status sp_check_args(const void* partials, int tp, int64_t T_pad, int64_t T_v
                         const void* out_scales, const void* residual_out);
 
 /*
+ * sp_fused_reduce_norm_host — the same stage, with every tensor argument (partials, residual,
+ * weight, bias, scale, out, out_scales, residual_out) in page-locked HOST memory (cudaHostAlloc
+ * or cudaHostRegister; device memory is accepted too). The kernel reads the inputs across the
+ * host link and writes the outputs back across it as it goes (zero-copy), so the host->device
+ * and device->host traffic of a call overlap each other and the computation, with no device
+ * staging buffers. Same arguments, checks, statuses and results as sp_fused_reduce_norm, plus
+ * SP_ERR_INVALID_ARG for a pointer the device cannot reach (pageable memory). Asynchronous on
+ * `stream`: synchronise the stream before reading the outputs on the host.
+ */
+sp_status sp_fused_reduce_norm_host(const void* partials, int tp, int64_t T_pad, int64_t T_valid,
+                                    int64_t H, const void* residual, const void* weight,
+                                    const void* bias, float eps, int quant_mode,
+                                    const float* scale, void* out, void* out_scales,
+                                    void* residual_out, sp_stream_t stream);
+
+/*
  * Launch configurations. sp_fused_reduce_norm picks one by itself (sp_select_launch tells
  * which); sp_fused_reduce_norm_with_config runs a given one, for tests and tuning. Every
  * configuration computes the same function.

@@ -19,7 +19,7 @@ import os
 from . import build as _build
 
 __all__ = [
-    "SpError", "QUANT_MODES", "load_library", "sp_fused_reduce_norm",
+    "SpError", "QUANT_MODES", "load_library", "sp_fused_reduce_norm", "sp_fused_reduce_norm_host",
     "sp_fused_reduce_norm_with_config", "sp_check_args", "sp_select_launch", "sp_pad_tokens",
     "sp_shard_rows", "sp_out_bytes", "sp_out_scales_bytes", "sp_max_hidden", "sp_status_string",
     "sp_device_error", "allocate_outputs", "LaunchConfig",
@@ -76,6 +76,8 @@ def load_library() -> ctypes.CDLL:
     lib.sp_fused_reduce_norm.restype = ctypes.c_int
     lib.sp_fused_reduce_norm_with_config.argtypes = [ctypes.POINTER(LaunchConfig)] + _MAIN_ARGS + [_vp]
     lib.sp_fused_reduce_norm_with_config.restype = ctypes.c_int
+    lib.sp_fused_reduce_norm_host.argtypes = _MAIN_ARGS + [_vp]
+    lib.sp_fused_reduce_norm_host.restype = ctypes.c_int
     lib.sp_check_args.argtypes = _MAIN_ARGS
     lib.sp_check_args.restype = ctypes.c_int
     lib.sp_select_launch.argtypes = [ctypes.c_int, _i64, _i64, ctypes.c_int,
@@ -140,6 +142,20 @@ def sp_fused_reduce_norm(partials, weight, out, residual_out, *, residual=None, 
     st = load_library().sp_fused_reduce_norm(*args, _stream_handle(stream))
     if st != 0:
         raise SpError(st, "sp_fused_reduce_norm")
+
+
+def sp_fused_reduce_norm_host(partials, weight, out, residual_out, *, residual=None, bias=None,
+                              eps: float = 1e-6, quant_mode="none", scale=None, out_scales=None,
+                              T_valid: int | None = None, stream=None) -> None:
+    """The stage on page-locked HOST tensors (``tensor.pin_memory()``): the kernel reads inputs
+    and writes outputs across the host link (zero-copy). ``scale`` is a pinned fp32 tensor with
+    one element, or None. Asynchronous on ``stream`` (default: torch's current CUDA stream);
+    synchronise before reading the outputs."""
+    args = _main_args(partials, residual, weight, bias, eps, quant_mode, scale, out, out_scales,
+                      residual_out, T_valid)
+    st = load_library().sp_fused_reduce_norm_host(*args, _stream_handle(stream))
+    if st != 0:
+        raise SpError(st, "sp_fused_reduce_norm_host")
 
 
 def sp_fused_reduce_norm_with_config(config: LaunchConfig | dict, partials, weight, out,

@@ -335,6 +335,54 @@ sp_status sp_fused_reduce_norm_with_config(const sp_launch_config* config, const
              scale, out, out_scales, residual_out, reinterpret_cast<cudaStream_t>(stream));
 }
 
+// Device address of a page-locked host (or device) buffer; false for memory the device cannot
+// reach (pageable) or an unknown pointer.
+static bool device_view(const void* p, const void** dev_ptr) {
+  if (!p) {
+    *dev_ptr = nullptr;
+    return true;
+  }
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  if (a.type == cudaMemoryTypeDevice || a.type == cudaMemoryTypeManaged) {
+    *dev_ptr = p;
+    return true;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return false;
+  // the same offset into the mapping as p has into its allocation
+  *dev_ptr = static_cast<const char*>(a.devicePointer) +
+             (static_cast<const char*>(p) - static_cast<const char*>(a.hostPointer));
+  return true;
+}
+
+sp_status sp_fused_reduce_norm_host(const void* partials, int tp, int64_t T_pad, int64_t T_valid,
+                                    int64_t H, const void* residual, const void* weight,
+                                    const void* bias, float eps, int quant_mode,
+                                    const float* scale, void* out, void* out_scales,
+                                    void* residual_out, sp_stream_t stream) {
+  sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode,
+                       scale, out, out_scales, residual_out);
+  if (st != SP_OK || T_pad == 0) return st;
+  const void* host[8] = {partials, residual, weight, bias, scale, out, out_scales, residual_out};
+  const void* dev[8];
+  for (int i = 0; i < 8; ++i)
+    if (!device_view(host[i], &dev[i])) return SP_ERR_INVALID_ARG;
+  // Plain 128-bit loads (the direct kernel): the host link, not HBM, bounds this call, and a few
+  // hundred KB of loads in flight per GPU cover its latency.
+  sp_launch_config cfg{};
+  cfg.kernel = SP_KERNEL_DIRECT;
+  cfg.vec_per_thread = consumer_threads(H, 2) > spk::kMaxConsumerThreads ? 4 : 2;
+  cfg.ctas_per_sm = 4;
+  cfg.stages = 0;
+  return run(cfg, dev[0], tp, T_pad, T_valid, H, dev[1], dev[2], dev[3], eps, quant_mode,
+             static_cast<const float*>(dev[4]), const_cast<void*>(dev[5]),
+             const_cast<void*>(dev[6]), const_cast<void*>(dev[7]),
+             reinterpret_cast<cudaStream_t>(stream));
+}
+
 sp_status sp_check_args(const void* partials, int tp, int64_t T_pad, int64_t T_valid, int64_t H,
                         const void* residual, const void* weight, const void* bias, float eps,
                         int quant_mode, const float* scale, const void* out,

@@ -39,6 +39,48 @@ def _view(mid: torch.Tensor, shape, dtype) -> torch.Tensor:
     return mid.view(dtype).view(shape)
 
 
+def _pinned(t):
+    return None if t is None else t.cpu().pin_memory()
+
+
+def run_gpu_host(inp: dict, *, fill: int = 0xA5, stream=None) -> dict:
+    """Run the zero-copy entry point on pinned host copies of ``inp`` into guard-banded pinned
+    host outputs pre-filled with ``fill``; returns numpy results."""
+    T_pad, H, mode = inp["T_pad"], inp["H"], inp["mode"]
+    hin = {k: _pinned(inp[k]) for k in ("partials", "residual", "weight", "bias")}
+    o_bytes = sp.sp_out_bytes(T_pad, H, mode)
+    s_bytes = sp.sp_out_scales_bytes(T_pad, H, mode)
+    oshape, odt, sshape, sdt = oracle.out_layout(T_pad, H, mode)
+    tdt = {np.uint16: torch.bfloat16, np.uint8: torch.uint8, np.float32: torch.float32}
+
+    def guarded(nbytes):
+        whole = torch.full((nbytes + 2 * GUARD,), CANARY, dtype=torch.uint8).pin_memory()
+        whole[GUARD:GUARD + nbytes].fill_(fill)
+        return whole, whole[GUARD:GUARD + nbytes]
+
+    out_w, out_m = guarded(o_bytes)
+    out = _view(out_m, oshape, tdt[odt])
+    sc_w = sc = None
+    if s_bytes:
+        sc_w, sc_m = guarded(s_bytes)
+        sc = _view(sc_m, sshape, tdt[sdt])
+    res_w, res_m = guarded(T_pad * H * 2)
+    res_out = _view(res_m, (T_pad, H), torch.bfloat16)
+    scale_t = (torch.tensor([inp["scale"]], dtype=torch.float32).pin_memory()
+               if inp["scale"] is not None else None)
+    sp.sp_fused_reduce_norm_host(hin["partials"], hin["weight"], out, res_out,
+                                 residual=hin["residual"], bias=hin["bias"], eps=inp["eps"],
+                                 quant_mode=mode, scale=scale_t, out_scales=sc,
+                                 T_valid=inp["T_valid"], stream=stream)
+    torch.cuda.synchronize()
+    for w in (out_w, sc_w, res_w):
+        if w is not None:
+            g = torch.cat([w[:GUARD], w[-GUARD:]])
+            assert bool((g == CANARY).all()), "write outside an output buffer"
+    return {"out": bits_of(out), "out_scales": None if sc is None else bits_of(sc),
+            "residual_out": bits_of(res_out)}
+
+
 def run_gpu(inp: dict, *, config: dict | None = None, fill: int = 0xA5, inplace: bool = False,
             stream=None) -> dict:
     """Run the library once on inputs ``inp`` (device tensors from synth.make_inputs) into

@@ -16,7 +16,7 @@ import torch
 import sequence_reduce_add_gb300 as sp
 from sequence_reduce_add_gb300 import synth
 
-from parity_util import compare, run_gpu, run_oracle
+from parity_util import compare, run_gpu, run_gpu_host, run_oracle
 
 pytestmark = pytest.mark.gpu
 
@@ -142,6 +142,30 @@ def test_full_size_workload(wi):
     inp = synth.make_inputs(w, device=DEV)
     stats = _check(inp)
     print(w["name"], stats)
+
+
+@pytest.mark.parametrize("wi,rows", [(1, None), (2, 330), (3, 330), (4, 330), (5, 330), (2, None)])
+def test_host_buffers_zero_copy(wi, rows):
+    """sp_fused_reduce_norm_host: inputs and outputs in pinned host memory."""
+    w = synth.workload(wi)
+    inp = synth.make_inputs(w, device=DEV) if rows is None else _small(w, rows=rows)
+    a = run_gpu_host(inp, fill=0xA5)
+    b = run_gpu_host(inp, fill=0x5A)
+    for k in ("out", "out_scales", "residual_out"):
+        if a[k] is not None:
+            assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+    compare(a, run_oracle(inp), inp)
+
+
+def test_host_entry_rejects_pageable_memory():
+    w = synth.workload(1)
+    inp = synth.make_inputs(w, device="cpu")  # pageable host tensors
+    outs = sp.allocate_outputs(inp["T_pad"], inp["H"], "none", "cpu")
+    with pytest.raises(sp.SpError) as e:
+        sp.sp_fused_reduce_norm_host(inp["partials"], inp["weight"], outs["out"],
+                                     outs["residual_out"], residual=inp["residual"],
+                                     bias=inp["bias"], T_valid=inp["T_valid"])
+    assert e.value.status == 1
 
 
 def test_no_device_wait_ran_out():
