@@ -47,6 +47,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.sp_oracle_check_args.restype = ctypes.c_int
     lib.sp_oracle_fused_reduce_norm_rows.argtypes = _ARGS + [_f64p, _i64, _i64]
     lib.sp_oracle_fused_reduce_norm_rows.restype = ctypes.c_int
+    lib.sp_oracle_fused_reduce_norm_rows_ex.argtypes = _ARGS + [_f64p, _i64, _i64, ctypes.c_float,
+                                                                 _u16p]
+    lib.sp_oracle_fused_reduce_norm_rows_ex.restype = ctypes.c_int
     for name, cin, cout in (("bf16_encode", _f64p, _u16p), ("bf16_decode", _u16p, _f64p),
                             ("e4m3_encode", _f64p, _u8p), ("e4m3_decode", _u8p, _f64p),
                             ("e2m1_encode", _f64p, _u8p), ("e2m1_decode", _u8p, _f64p)):
@@ -81,13 +84,15 @@ def fused_reduce_norm(partials: np.ndarray, residual: np.ndarray | None, weight:
                       bias: np.ndarray | None, eps: float, mode: str, scale: float | None,
                       T_valid: int, *, want_y: bool = False, rows: tuple[int, int] | None = None,
                       threads: int = 1, lib: ctypes.CDLL | None = None,
-                      buffers: dict | None = None) -> dict:
+                      buffers: dict | None = None, partial_scale: float = 1.0,
+                      addend: np.ndarray | None = None) -> dict:
     """Run the oracle over rows ``rows`` (default all) of a [tp, T_pad, H] problem.
 
     Returns a dict with ``status``, ``out``, ``out_scales`` (or None), ``residual_out`` and, when
     ``want_y``, the unrounded fp64 ``y`` [T_pad, H]. Rows outside ``rows`` are left zero, unless
     ``buffers`` (a previous result) is given: its arrays are then reused and only ``rows`` of
-    them are rewritten.
+    them are rewritten. ``partial_scale`` multiplies every partial before the reduction;
+    ``addend`` (bf16 bits [T_pad, H]) is added after it, before the norm.
     """
     lib = lib or load()
     tp, T_pad, H = partials.shape
@@ -112,8 +117,15 @@ def fused_reduce_norm(partials: np.ndarray, residual: np.ndarray | None, weight:
     begin, end = rows if rows is not None else (0, T_pad)
     status = [0]
 
+    extended = partial_scale != 1.0 or addend is not None
+
     def run(b, e, slot):
-        st = lib.sp_oracle_fused_reduce_norm_rows(*args, _ptr(y, ctypes.c_double), b, e)
+        if extended:
+            st = lib.sp_oracle_fused_reduce_norm_rows_ex(
+                *args, _ptr(y, ctypes.c_double), b, e, ctypes.c_float(partial_scale),
+                _ptr(addend, ctypes.c_uint16))
+        else:
+            st = lib.sp_oracle_fused_reduce_norm_rows(*args, _ptr(y, ctypes.c_double), b, e)
         if st != 0:
             status[slot] = st
 

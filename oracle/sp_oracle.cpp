@@ -148,6 +148,8 @@ double as_fp32(double v) { return static_cast<double>(static_cast<float>(v)); }
 // sees them, plus the mode rules of [SP-Q] §四.
 // ---------------------------------------------------------------------------------------------
 struct Args {
+  float partial_scale;        // multiplies every partial before the reduction (1 = none)
+  const uint16_t* addend;     // bf16 [T_pad][H] added after the reduction, or null
   const uint16_t* partials;
   int tp;
   int64_t T_pad;
@@ -200,12 +202,13 @@ int validate(const Args& a) {
   if ((a.mode == kFp8PerToken || a.mode == kNvfp4) && !a.out_scales) return kInvalidArg;
   // Outputs must not overlap any input or each other; residual_out may be residual itself.
   const int64_t rows = a.T_pad * a.H * 2;
-  const void* inputs[] = {a.partials, a.residual, a.weight, a.bias, a.scale};
-  const int64_t in_n[] = {rows * a.tp, rows, a.H * 2, a.H * 2, 4};
+  if (!std::isfinite(a.partial_scale)) return kInvalidArg;
+  const void* inputs[] = {a.partials, a.residual, a.weight, a.bias, a.scale, a.addend};
+  const int64_t in_n[] = {rows * a.tp, rows, a.H * 2, a.H * 2, 4, rows};
   const void* outputs[] = {a.out, a.out_scales, a.residual_out};
   const int64_t out_n[] = {out_bytes(a), scale_bytes(a), rows};
   for (int o = 0; o < 3; ++o) {
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < 6; ++i) {
       if (o == 2 && i == 1 && a.residual_out == static_cast<const void*>(a.residual)) continue;
       if (overlaps(outputs[o], out_n[o], inputs[i], in_n[i])) return kInvalidArg;
     }
@@ -253,14 +256,19 @@ void one_row(const Args& a, int64_t t, double* y_out) {
   }
   std::vector<double> h(static_cast<size_t>(H)), y(static_cast<size_t>(H));
 
-  // (1) reduction over the tp partial sums, r = 0 .. tp-1
-  // (2) h = reduced + bias + residual (a missing bias or residual counts as zero)
+  // (1) reduction over the tp partial sums, r = 0 .. tp-1, each partial scaled first (a scale
+  //     applied before the reduction: PR #18671 notes §5.3)
+  // (2) h = reduced + bias + residual + addend (a missing term counts as zero; the addend is the
+  //     per-shard extra input added between the ReduceScatter and the norm, SP/FlashComm notes
+  //     §2.3, Qwen3-VL deepstack rewrite)
+  const double ps = static_cast<double>(a.partial_scale);
   for (int64_t j = 0; j < H; ++j) {
     double s = 0.0;
-    for (int r = 0; r < a.tp; ++r) s += bf16_value(a.partials[(r * a.T_pad + t) * H + j]);
+    for (int r = 0; r < a.tp; ++r) s += ps * bf16_value(a.partials[(r * a.T_pad + t) * H + j]);
     const double b = a.bias ? bf16_value(a.bias[j]) : 0.0;
     const double res = a.residual ? bf16_value(a.residual[t * H + j]) : 0.0;
-    h[j] = s + b + res;
+    const double add = a.addend ? bf16_value(a.addend[t * H + j]) : 0.0;
+    h[j] = s + b + res + add;
   }
 
   // (3) the new residual is h rounded once to bf16 (read of row t above is complete, so
@@ -315,9 +323,10 @@ void one_row(const Args& a, int64_t t, double* y_out) {
 
 Args make_args(const uint16_t* partials, int tp, int64_t T_pad, int64_t T_valid, int64_t H,
                const uint16_t* residual, const uint16_t* weight, const uint16_t* bias, float eps,
-               int mode, const float* scale, void* out, void* out_scales, uint16_t* residual_out) {
-  return Args{partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, mode, scale,
-              out, out_scales, residual_out};
+               int mode, const float* scale, void* out, void* out_scales, uint16_t* residual_out,
+               float partial_scale = 1.0f, const uint16_t* addend = nullptr) {
+  return Args{partial_scale, addend, partials, tp, T_pad, T_valid, H, residual, weight, bias, eps,
+              mode, scale, out, out_scales, residual_out};
 }
 
 }  // namespace
@@ -348,6 +357,24 @@ int sp_oracle_fused_reduce_norm_rows(const uint16_t* partials, int tp, int64_t T
                                      int64_t row_begin, int64_t row_end) {
   const Args a = make_args(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode,
                            scale, out, out_scales, residual_out);
+  const int st = validate(a);
+  if (st != kOk) return st;
+  if (row_begin < 0 || row_end > T_pad || row_begin > row_end) return kInvalidArg;
+  for (int64_t t = row_begin; t < row_end; ++t) one_row(a, t, y_out);
+  return kOk;
+}
+
+// As sp_oracle_fused_reduce_norm_rows, with a scale applied to every partial before the
+// reduction and an optional addend [T_pad][H] added after it (before the norm).
+int sp_oracle_fused_reduce_norm_rows_ex(const uint16_t* partials, int tp, int64_t T_pad,
+                                        int64_t T_valid, int64_t H, const uint16_t* residual,
+                                        const uint16_t* weight, const uint16_t* bias, float eps,
+                                        int quant_mode, const float* scale, void* out,
+                                        void* out_scales, uint16_t* residual_out, double* y_out,
+                                        int64_t row_begin, int64_t row_end, float partial_scale,
+                                        const uint16_t* addend) {
+  const Args a = make_args(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode,
+                           scale, out, out_scales, residual_out, partial_scale, addend);
   const int st = validate(a);
   if (st != kOk) return st;
   if (row_begin < 0 || row_end > T_pad || row_begin > row_end) return kInvalidArg;

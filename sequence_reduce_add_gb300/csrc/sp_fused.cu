@@ -143,11 +143,50 @@ int max_stages(int64_t H, int ctas_per_sm) {
 // Grid of a persistent launch: SMs x CTAs per SM, where CTAs per SM is the requested number
 // capped at what the SM can hold for this kernel (registers, threads, shared memory), so the
 // grid is never a ragged second wave; and never more CTAs than rows.
+// Resident CTAs per SM of (kernel, threads, smem) on the current device, cached: the occupancy
+// query costs about a microsecond, as much as the launch of a small problem.
+struct OccupancyKey {
+  const void* kernel;
+  int device, threads, smem;
+};
+constexpr int kOccupancySlots = 256;
+OccupancyKey g_occ_keys[kOccupancySlots];
+int g_occ_values[kOccupancySlots];
+int g_occ_used = 0;
+std::mutex g_occ_mutex;
+
+template <typename Kernel>
+cudaError_t resident_ctas(Kernel kernel, int threads, int smem, int* resident) {
+  int device = 0;
+  cudaError_t e = cudaGetDevice(&device);
+  if (e != cudaSuccess) return e;
+  const void* k = reinterpret_cast<const void*>(kernel);
+  {
+    std::lock_guard<std::mutex> lock(g_occ_mutex);
+    for (int i = 0; i < g_occ_used; ++i) {
+      const OccupancyKey& c = g_occ_keys[i];
+      if (c.kernel == k && c.device == device && c.threads == threads && c.smem == smem) {
+        *resident = g_occ_values[i];
+        return cudaSuccess;
+      }
+    }
+  }
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(resident, kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(g_occ_mutex);
+  if (g_occ_used < kOccupancySlots) {
+    g_occ_keys[g_occ_used] = OccupancyKey{k, device, threads, smem};
+    g_occ_values[g_occ_used] = *resident;
+    ++g_occ_used;
+  }
+  return cudaSuccess;
+}
+
 template <typename Kernel>
 cudaError_t persistent_grid(Kernel kernel, int threads, int smem, int ctas_per_sm,
                             int64_t rows, const DeviceInfo* dev, int* grid) {
   int resident = 0;
-  cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&resident, kernel, threads, smem);
+  cudaError_t e = resident_ctas(kernel, threads, smem, &resident);
   if (e != cudaSuccess) return e;
   if (resident < 1) return cudaErrorInvalidConfiguration;
   const int per_sm = ctas_per_sm < resident ? ctas_per_sm : resident;

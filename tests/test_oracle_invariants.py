@@ -388,3 +388,75 @@ def test_argument_rules():
     assert st(residual_out_ptr=A * 8 + 16) == "invalid_arg"  # partial overlap
     assert st(out_ptr=A + 64) == "invalid_arg"    # output inside the partials
     assert st(T_pad=0, T_valid=0, partials_ptr=None) == "ok"
+
+
+# --------------------------------------------------------------------------- N3 extensions
+def run_ex(partials, residual, weight, bias, mode, T_valid, partial_scale=1.0, addend=None,
+           eps=1e-6, **kw):
+    res = oracle.fused_reduce_norm(
+        bits(partials), None if residual is None else bits(residual), bits(weight),
+        None if bias is None else bits(bias), eps, mode, scale_for(mode), T_valid,
+        partial_scale=partial_scale, addend=None if addend is None else bits(addend), **kw)
+    assert res["status"] == 0
+    return res
+
+
+@pytest.mark.parametrize("mode", MODES)
+@pytest.mark.parametrize("c", [0.5, 2.0, 0.25, -1.0])
+def test_partial_scale_multiplies_each_partial_before_the_sum(mode, c):
+    # a scale applied to every partial before the reduction (PR #18671 notes §5.3) is the
+    # same as feeding already-scaled partials: exact here (integers times powers of two)
+    g = torch.Generator().manual_seed(61)
+    tp, T, H = 4, 8, 32
+    partials = ints(g, (tp, T, H), -8, 8)
+    residual, bias = ints(g, (T, H), -8, 8), ints(g, (H,), -2, 2)
+    w = rand_bf16(g, (H,), 0.2) + 1
+    scaled = (partials.double() * c).to(torch.bfloat16)
+    assert torch.equal(scaled.double(), partials.double() * c)
+    same(run_ex(partials, residual, w, bias, mode, T - 1, partial_scale=c),
+         run_ex(scaled, residual, w, bias, mode, T - 1))
+
+
+def test_partial_scale_matches_torch_rms_norm():
+    g = torch.Generator().manual_seed(62)
+    T, H, c = 9, 128, 1.0 / 3.0
+    x = rand_bf16(g, (1, T, H), 0.7)
+    res = rand_bf16(g, (T, H))
+    w = rand_bf16(g, (H,), 0.2) + 1
+    c32 = float(np.float32(c))
+    y = run_ex(x, res, w, None, "none", T, partial_scale=c, eps=1e-3, want_y=True)["y"]
+    want = torch.nn.functional.rms_norm(c32 * x[0].double() + res.double(), (H,), w.double(),
+                                        eps=float(np.float32(1e-3)))
+    np.testing.assert_allclose(y, want.numpy(), rtol=1e-13, atol=0)
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_addend_is_added_like_the_residual(mode):
+    g = torch.Generator().manual_seed(63)
+    tp, T, H = 2, 6, 48
+    partials = ints(g, (tp, T, H), -8, 8)
+    residual, addend, bias = ints(g, (T, H), -8, 8), ints(g, (T, H), -8, 8), ints(g, (H,), -2, 2)
+    w = rand_bf16(g, (H,), 0.2) + 1
+    both = (residual.double() + addend.double()).to(torch.bfloat16)
+    same(run_ex(partials, residual, w, bias, mode, T - 1, addend=addend),
+         run_ex(partials, both, w, bias, mode, T - 1))
+    # without a residual the addend alone plays its part
+    same(run_ex(partials, None, w, bias, mode, T, addend=addend),
+         run_ex(partials, addend, w, bias, mode, T))
+
+
+@pytest.mark.parametrize("mode", MODES)
+def test_addend_is_chunked_per_shard(mode):
+    # reduce_scatter -> add(chunk(addend)[rank]) -> norm -> all_gather (SP/FlashComm notes §2.3)
+    g = torch.Generator().manual_seed(64)
+    tp, S, H = 4, 4, 32
+    T = tp * S
+    partials = rand_bf16(g, (tp, T, H), 0.5)
+    residual, addend = rand_bf16(g, (T, H)), rand_bf16(g, (T, H), 0.3)
+    w, b = rand_bf16(g, (H,), 0.1) + 1, rand_bf16(g, (H,), 0.01)
+    full = run_ex(partials, residual, w, b, mode, T - 3, partial_scale=0.75, addend=addend)
+    shards = [run_ex(partials[:, r * S:(r + 1) * S].contiguous(),
+                     residual[r * S:(r + 1) * S].contiguous(), w, b, mode,
+                     max(0, min(S, T - 3 - r * S)), partial_scale=0.75,
+                     addend=addend[r * S:(r + 1) * S].contiguous()) for r in range(tp)]
+    same(full, concat(shards))

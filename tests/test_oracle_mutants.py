@@ -20,9 +20,14 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 MUTANTS = {
     "drop_last_partial": ("for (int r = 0; r < a.tp; ++r)", "for (int r = 0; r < a.tp - 1; ++r)"),
     "transposed_partials": ("a.partials[(r * a.T_pad + t) * H + j]", "a.partials[(t * a.tp + r) * H + j]"),
-    "drop_bias": ("h[j] = s + b + res;", "h[j] = s + res + 0 * b;"),
-    "drop_residual": ("h[j] = s + b + res;", "h[j] = s + b + 0 * res;"),
-    "bias_sign": ("h[j] = s + b + res;", "h[j] = s - b + res;"),
+    "drop_bias": ("h[j] = s + b + res + add;", "h[j] = s + res + add + 0 * b;"),
+    "drop_residual": ("h[j] = s + b + res + add;", "h[j] = s + b + add + 0 * res;"),
+    "bias_sign": ("h[j] = s + b + res + add;", "h[j] = s - b + res + add;"),
+    "drop_addend": ("h[j] = s + b + res + add;", "h[j] = s + b + res + 0 * add;"),
+    "addend_row_index": ("a.addend[t * H + j]", "a.addend[j]"),
+    "partial_scale_ignored": ("s += ps * bf16_value(", "s += bf16_value("),
+    "partial_scale_on_everything": ("h[j] = s + b + res + add;",
+                                    "h[j] = s + ps * (b + res + add);"),
     "residual_row_index": ("a.residual[t * H + j]", "a.residual[j]"),
     "eps_outside_sqrt": ("1.0 / std::sqrt(mean_sq + static_cast<double>(a.eps))",
                          "1.0 / (std::sqrt(mean_sq) + static_cast<double>(a.eps))"),
