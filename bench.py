@@ -46,13 +46,13 @@ L2_BYTES = 129 * 1024 * 1024
 
 # ------------------------------------------------------------------------------ workload math
 def algorithmic_bytes(tp: int, T_valid: int, T_pad: int, H: int, mode: str,
-                      residual: bool = True) -> int:
-    """Bytes one call must move: per valid row tp partial rows + the residual row read (2H each)
-    and residual_out + out (+ scales) written; per padding row the zero writes only. Weight and
-    bias (2H each, read once per CTA and L2-resident) are left out."""
+                      residual: bool = True, addend: bool = False) -> int:
+    """Bytes one call must move: per valid row tp partial rows + the residual row (+ the addend
+    row) read (2H each) and residual_out + out (+ scales) written; per padding row the zero writes
+    only. Weight and bias (2H each, read once per CTA and L2-resident) are left out."""
     out_row = {"none": 2 * H, "fp8_static": H, "fp8_per_token": H + 4,
                "nvfp4": H // 2 + H // 16}[mode]
-    read_row = 2 * H * (tp + (1 if residual else 0))
+    read_row = 2 * H * (tp + (1 if residual else 0) + (1 if addend else 0))
     write_row = 2 * H + out_row
     return T_valid * (read_row + write_row) + (T_pad - T_valid) * write_row
 
@@ -152,12 +152,22 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------------------ our arm
+VARIANTS = {
+    # "First" layer of the quant-aware SP patterns: no incoming residual
+    "first": dict(with_residual=False),
+    # a scale on every partial before the reduction plus a per-shard addend after it
+    "scaled_addend": dict(with_addend=True, partial_scale=0.5),
+}
+
+
 class Problem:
     """One resident input/output set of a workload, with prebuilt C-ABI argument tuples."""
 
-    def __init__(self, w: dict, seed: int, device, sp):
+    def __init__(self, w: dict, seed: int, device, sp, variant: str | None = None):
         from sequence_reduce_add_gb300 import synth
-        self.inp = synth.make_inputs(w, seed=seed, device=device)
+        v = dict(VARIANTS.get(variant, {}))
+        partial_scale = v.pop("partial_scale", 1.0)
+        self.inp = synth.make_inputs(w, seed=seed, device=device, **v)
         i = self.inp
         self.outs = sp.allocate_outputs(i["T_pad"], i["H"], i["mode"], device)
         self.scale = (torch.tensor([i["scale"]], dtype=torch.float32, device=device)
@@ -167,9 +177,16 @@ class Problem:
                      p(i["weight"]), p(i["bias"]), ctypes.c_float(i["eps"]),
                      sp.QUANT_MODES[i["mode"]], p(self.scale), p(self.outs["out"]),
                      p(self.outs["out_scales"]), p(self.outs["residual_out"]))
+        self.fn_name = "sp_fused_reduce_norm"
+        if variant is not None:  # the options entry point
+            self.options = sp.sp_options_init(partial_scale=partial_scale, addend=i["addend"])
+            self.args = (ctypes.byref(self.options),) + self.args
+            self.fn_name = "sp_fused_reduce_norm_ex"
+        self.bytes = algorithmic_bytes(i["tp"], i["T_valid"], i["T_pad"], i["H"], i["mode"],
+                                       i["residual"] is not None, i["addend"] is not None)
 
     def nbytes(self) -> int:
-        ts = [self.inp["partials"], self.inp["residual"], self.outs["out"],
+        ts = [self.inp["partials"], self.inp["residual"], self.inp["addend"], self.outs["out"],
               self.outs["out_scales"], self.outs["residual_out"]]
         return sum(t.numel() * t.element_size() for t in ts if t is not None)
 
@@ -180,7 +197,7 @@ def time_kernel_loop(lib, problems, steps: int, stream, per_launch_events: bool)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)] if per_launch_events else None)
-    fn = lib.sp_fused_reduce_norm
+    fn = getattr(lib, problems[0].fn_name)
     n = len(problems)
     start.record(stream)
     for s in range(steps):
@@ -188,7 +205,7 @@ def time_kernel_loop(lib, problems, steps: int, stream, per_launch_events: bool)
             ev[s][0].record(stream)
         st = fn(*problems[s % n].args, handle)
         if st != 0:
-            raise RuntimeError(f"sp_fused_reduce_norm returned {st}")
+            raise RuntimeError(f"{problems[0].fn_name} returned {st}")
         if ev:
             ev[s][1].record(stream)
     end.record(stream)
@@ -399,6 +416,9 @@ def run_ours(args) -> None:
             if other["name"] == w["name"]:
                 continue
             extras[other["name"]] = bench_extra(lib, sp, synth, other, device, stream, peak)
+        for variant in VARIANTS:
+            extras[f"{w['name']}+{variant}"] = bench_extra(lib, sp, synth, w, device, stream,
+                                                           peak, variant)
 
     if rank != 0:
         return
@@ -437,13 +457,13 @@ def run_ours(args) -> None:
     print(json.dumps(line), flush=True)
 
 
-def bench_extra(lib, sp, synth, w, device, stream, peak) -> dict:
+def bench_extra(lib, sp, synth, w, device, stream, peak, variant: str | None = None) -> dict:
     """Per-workload kernel figures for the other workloads (rotating sets, CUDA events)."""
-    base = Problem(w, synth.BASE_SEED + 1 + synth.WORKLOADS.index(w), device, sp)
+    base = Problem(w, synth.BASE_SEED + 1 + synth.WORKLOADS.index(w), device, sp, variant)
     sets = max(2, min(6, -(-(4 * L2_BYTES) // base.nbytes())))
-    problems = [base] + [Problem(w, base.inp["seed"] + 1000 * k, device, sp)
+    problems = [base] + [Problem(w, base.inp["seed"] + 1000 * k, device, sp, variant)
                          for k in range(1, sets)]
-    one = algorithmic_bytes(w["tp"], w["T_valid"], w["T_pad"], w["H"], w["mode"])
+    one = base.bytes
     steps = max(20, int(0.25e9 / max(one, 1)) * 4)
     steps = min(steps, 4000)
     time_kernel_loop(lib, problems, 10, stream, False)

@@ -127,6 +127,50 @@ sp_status sp_check_args(const void* partials, int tp, int64_t T_pad, int64_t T_v
                         const void* out_scales, const void* residual_out);
 
 /*
+ * Options of sp_fused_reduce_norm_ex. Initialise with sp_options_init (which gives exactly
+ * sp_fused_reduce_norm) and change what is needed.
+ *   partial_scale  every partial is multiplied by this before the reduction (a per-rank output
+ *                  scale applied before the ReduceScatter, PR #18671 notes §5.3): finite; 1 = none.
+ *   addend         bf16 [T_pad][H] added after the reduction and before the norm, and so also
+ *                  part of the new residual: h = partial_scale * sum_r partials[r][t] + bias +
+ *                  residual[t] + addend[t] (the per-shard extra input of the Qwen3-VL deepstack
+ *                  rewrite, vllm-ascend SP notes §2.3); NULL = none. Never read on padding rows.
+ *   scale_layout   NVFP4 block scales: SP_SCALES_ROW_MAJOR ([T_pad][H/16]); other values are
+ *                  SP_ERR_UNSUPPORTED.
+ *   host_buffers   0: every tensor is in device memory; 1: tensors are in page-locked host memory
+ *                  (or device memory) and are read/written across the host link (zero-copy).
+ */
+enum { SP_SCALES_ROW_MAJOR = 0 };
+
+typedef struct sp_fused_options {
+  float partial_scale;
+  const void* addend;
+  int scale_layout;
+  int host_buffers;
+} sp_fused_options;
+
+void sp_options_init(sp_fused_options* options /* host, out */);
+
+/*
+ * sp_fused_reduce_norm_ex — sp_fused_reduce_norm with options (NULL options = defaults). The
+ * addend follows the same rules as the residual (16-byte aligned, may not overlap an output).
+ * A non-finite partial_scale is SP_ERR_INVALID_ARG.
+ */
+sp_status sp_fused_reduce_norm_ex(const sp_fused_options* options /* host */,
+                                  const void* partials, int tp, int64_t T_pad, int64_t T_valid,
+                                  int64_t H, const void* residual, const void* weight,
+                                  const void* bias, float eps, int quant_mode, const float* scale,
+                                  void* out, void* out_scales, void* residual_out,
+                                  sp_stream_t stream);
+
+/* sp_check_args_ex — the checks of sp_fused_reduce_norm_ex alone (no GPU needed). */
+sp_status sp_check_args_ex(const sp_fused_options* options /* host */, const void* partials,
+                           int tp, int64_t T_pad, int64_t T_valid, int64_t H, const void* residual,
+                           const void* weight, const void* bias, float eps, int quant_mode,
+                           const float* scale, const void* out, const void* out_scales,
+                           const void* residual_out);
+
+/*
  * sp_fused_reduce_norm_host — the same stage, with every tensor argument (partials, residual,
  * weight, bias, scale, out, out_scales, residual_out) in page-locked HOST memory (cudaHostAlloc
  * or cudaHostRegister; device memory is accepted too). The kernel reads the inputs across the

@@ -22,7 +22,8 @@ __all__ = [
     "SpError", "QUANT_MODES", "load_library", "sp_fused_reduce_norm", "sp_fused_reduce_norm_host",
     "sp_fused_reduce_norm_with_config", "sp_check_args", "sp_select_launch", "sp_pad_tokens",
     "sp_shard_rows", "sp_out_bytes", "sp_out_scales_bytes", "sp_max_hidden", "sp_status_string",
-    "sp_device_error", "allocate_outputs", "LaunchConfig",
+    "sp_device_error", "allocate_outputs", "LaunchConfig", "Options", "sp_options_init",
+    "sp_fused_reduce_norm_ex", "sp_check_args_ex",
 ]
 
 QUANT_MODES = {"none": 0, "fp8_static": 1, "fp8_per_token": 2, "nvfp4": 3,
@@ -41,6 +42,13 @@ class SpError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
         super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
+
+
+class Options(ctypes.Structure):
+    """sp_fused_options: partial_scale, addend (device address or None), scale_layout,
+    host_buffers."""
+    _fields_ = [("partial_scale", ctypes.c_float), ("addend", ctypes.c_void_p),
+                ("scale_layout", ctypes.c_int), ("host_buffers", ctypes.c_int)]
 
 
 class LaunchConfig(ctypes.Structure):
@@ -76,6 +84,12 @@ def load_library() -> ctypes.CDLL:
     lib.sp_fused_reduce_norm.restype = ctypes.c_int
     lib.sp_fused_reduce_norm_with_config.argtypes = [ctypes.POINTER(LaunchConfig)] + _MAIN_ARGS + [_vp]
     lib.sp_fused_reduce_norm_with_config.restype = ctypes.c_int
+    lib.sp_options_init.argtypes = [ctypes.POINTER(Options)]
+    lib.sp_options_init.restype = None
+    lib.sp_fused_reduce_norm_ex.argtypes = [ctypes.POINTER(Options)] + _MAIN_ARGS + [_vp]
+    lib.sp_fused_reduce_norm_ex.restype = ctypes.c_int
+    lib.sp_check_args_ex.argtypes = [ctypes.POINTER(Options)] + _MAIN_ARGS
+    lib.sp_check_args_ex.restype = ctypes.c_int
     lib.sp_fused_reduce_norm_host.argtypes = _MAIN_ARGS + [_vp]
     lib.sp_fused_reduce_norm_host.restype = ctypes.c_int
     lib.sp_check_args.argtypes = _MAIN_ARGS
@@ -142,6 +156,42 @@ def sp_fused_reduce_norm(partials, weight, out, residual_out, *, residual=None, 
     st = load_library().sp_fused_reduce_norm(*args, _stream_handle(stream))
     if st != 0:
         raise SpError(st, "sp_fused_reduce_norm")
+
+
+def sp_options_init(*, partial_scale: float = 1.0, addend=None, scale_layout: int = 0,
+                    host_buffers: bool = False) -> Options:
+    """An sp_fused_options initialised by the library, then set from the keywords (``addend`` is a
+    tensor or None)."""
+    o = Options()
+    load_library().sp_options_init(ctypes.byref(o))
+    o.partial_scale = partial_scale
+    o.addend = _ptr(addend)
+    o.scale_layout = scale_layout
+    o.host_buffers = 1 if host_buffers else 0
+    return o
+
+
+def sp_fused_reduce_norm_ex(options: Options | None, partials, weight, out, residual_out, *,
+                            residual=None, bias=None, eps: float = 1e-6, quant_mode="none",
+                            scale=None, out_scales=None, T_valid: int | None = None,
+                            stream=None) -> None:
+    """``sp_fused_reduce_norm`` with options (``sp_options_init``): a scale applied to every
+    partial before the reduction, an addend after it, host buffers."""
+    args = _main_args(partials, residual, weight, bias, eps, quant_mode, scale, out, out_scales,
+                      residual_out, T_valid)
+    st = load_library().sp_fused_reduce_norm_ex(
+        ctypes.byref(options) if options is not None else None, *args, _stream_handle(stream))
+    if st != 0:
+        raise SpError(st, "sp_fused_reduce_norm_ex")
+
+
+def sp_check_args_ex(options: Options | None, partials, tp, T_pad, T_valid, H, residual, weight,
+                     bias, eps, quant_mode, scale, out, out_scales, residual_out) -> int:
+    """The checks of sp_fused_reduce_norm_ex on raw addresses; returns the status."""
+    return load_library().sp_check_args_ex(
+        ctypes.byref(options) if options is not None else None, partials, tp, T_pad, T_valid, H,
+        residual, weight, bias, ctypes.c_float(eps), _mode(quant_mode), scale, out, out_scales,
+        residual_out)
 
 
 def sp_fused_reduce_norm_host(partials, weight, out, residual_out, *, residual=None, bias=None,

@@ -23,6 +23,8 @@ constexpr unsigned int kErrWaitTimeout = 1u;
 struct Params {
   const uint16_t* partials;   // bf16 [tp][T_pad][H]
   const uint16_t* residual;   // bf16 [T_pad][H] or null
+  const uint16_t* addend;     // bf16 [T_pad][H] or null: added after the reduction
+  float partial_scale;        // multiplies the sum of the partials (1 = none)
   const uint16_t* weight;     // bf16 [H]
   const uint16_t* bias;       // bf16 [H] or null
   const float* scale;         // fp32 [1] or null

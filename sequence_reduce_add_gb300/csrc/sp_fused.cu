@@ -46,10 +46,16 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 // The checks of sp_fused_reduce_norm, in the documented order. The shape rules restate the
 // shard checks of the PR #18671 notes (§5.2): the padded token count is a whole number of
 // equal shards, and the valid tokens fit in it.
+// What sp_fused_reduce_norm_ex adds to the plain call (defaults: 1 and none).
+struct Extras {
+  float partial_scale = 1.0f;
+  const void* addend = nullptr;
+};
+
 sp_status check(const void* partials, int tp, int64_t T_pad, int64_t T_valid, int64_t H,
                 const void* residual, const void* weight, const void* bias, float eps, int mode,
                 const float* scale, const void* out, const void* out_scales,
-                const void* residual_out) {
+                const void* residual_out, const Extras& x = Extras()) {
   if (mode == SP_QUANT_FP8_DYNAMIC_PER_TENSOR) return SP_ERR_UNSUPPORTED;
   if (mode < SP_QUANT_NONE || mode > SP_QUANT_NVFP4) return SP_ERR_INVALID_ARG;
   if (tp < 1 || T_pad < 0 || T_valid < 0 || T_valid > T_pad) return SP_ERR_INVALID_ARG;
@@ -57,25 +63,27 @@ sp_status check(const void* partials, int tp, int64_t T_pad, int64_t T_valid, in
   if (H <= 0 || H % 8 != 0) return SP_ERR_INVALID_ARG;
   if (mode == SP_QUANT_NVFP4 && H % 16 != 0) return SP_ERR_INVALID_ARG;
   if (!(eps > 0.0f) || !std::isfinite(eps)) return SP_ERR_INVALID_ARG;
+  if (!std::isfinite(x.partial_scale)) return SP_ERR_INVALID_ARG;
   if (T_pad == 0) return SP_OK;
   if (!partials || !weight || !out || !residual_out) return SP_ERR_INVALID_ARG;
   if ((mode == SP_QUANT_FP8_STATIC || mode == SP_QUANT_NVFP4) && !scale) return SP_ERR_INVALID_ARG;
   if ((mode == SP_QUANT_FP8_PER_TOKEN || mode == SP_QUANT_NVFP4) && !out_scales)
     return SP_ERR_INVALID_ARG;
   const int64_t rows = T_pad * H * 2;
-  const void* inputs[] = {partials, residual, weight, bias, scale};
-  const int64_t in_n[] = {rows * tp, rows, H * 2, H * 2, 4};
+  const void* inputs[] = {partials, residual, weight, bias, scale, x.addend};
+  const int64_t in_n[] = {rows * tp, rows, H * 2, H * 2, 4, rows};
   const void* outputs[] = {out, out_scales, residual_out};
   const int64_t out_n[] = {out_bytes_of(T_pad, H, mode), scale_bytes_of(T_pad, H, mode), rows};
   for (int o = 0; o < 3; ++o) {
-    for (int i = 0; i < 5; ++i) {
+    for (int i = 0; i < 6; ++i) {
       if (o == 2 && i == 1 && residual_out == residual) continue;  // in-place residual update
       if (overlaps(outputs[o], out_n[o], inputs[i], in_n[i])) return SP_ERR_INVALID_ARG;
     }
     for (int q = o + 1; q < 3; ++q)
       if (overlaps(outputs[o], out_n[o], outputs[q], out_n[q])) return SP_ERR_INVALID_ARG;
   }
-  const void* all[] = {partials, residual, weight, bias, scale, out, out_scales, residual_out};
+  const void* all[] = {partials, residual, weight, bias,         scale,
+                       out,      out_scales, residual_out, x.addend};
   for (const void* ptr : all)
     if (ptr && !aligned16(ptr)) return SP_ERR_ALIGNMENT;
   if (H > kMaxHidden) return SP_ERR_UNSUPPORTED;
@@ -267,14 +275,13 @@ sp_status config_is_valid(const sp_launch_config& cfg, int64_t H) {
   return SP_OK;
 }
 
-sp_status run(const sp_launch_config& cfg_in, const void* partials, int tp, int64_t T_pad,
-              int64_t T_valid, int64_t H, const void* residual, const void* weight,
-              const void* bias, float eps, int mode, const float* scale, void* out,
-              void* out_scales, void* residual_out, cudaStream_t stream) {
-  sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, mode, scale,
-                       out, out_scales, residual_out);
-  if (st != SP_OK) return st;
-  st = config_is_valid(cfg_in, H);
+// Launch after the checks have passed.
+sp_status run_checked(const sp_launch_config& cfg_in, const void* partials, int tp, int64_t T_pad,
+                      int64_t T_valid, int64_t H, const void* residual, const void* weight,
+                      const void* bias, float eps, int mode, const float* scale, void* out,
+                      void* out_scales, void* residual_out, cudaStream_t stream,
+                      const Extras& x) {
+  sp_status st = config_is_valid(cfg_in, H);
   if (st != SP_OK) return st;
   if (T_pad == 0) return SP_OK;
   DeviceInfo* dev = nullptr;
@@ -285,6 +292,8 @@ sp_status run(const sp_launch_config& cfg_in, const void* partials, int tp, int6
   spk::Params p{};
   p.partials = static_cast<const uint16_t*>(partials);
   p.residual = static_cast<const uint16_t*>(residual);
+  p.addend = static_cast<const uint16_t*>(x.addend);
+  p.partial_scale = x.partial_scale;
   p.weight = static_cast<const uint16_t*>(weight);
   p.bias = static_cast<const uint16_t*>(bias);
   p.scale = scale;
@@ -315,6 +324,18 @@ sp_status run(const sp_launch_config& cfg_in, const void* partials, int tp, int6
     default: e = launch_mode<4>(mode, cfg, p, smem, stream, dev); break;
   }
   return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
+sp_status run(const sp_launch_config& cfg, const void* partials, int tp, int64_t T_pad,
+              int64_t T_valid, int64_t H, const void* residual, const void* weight,
+              const void* bias, float eps, int mode, const float* scale, void* out,
+              void* out_scales, void* residual_out, cudaStream_t stream,
+              const Extras& x = Extras()) {
+  const sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, mode,
+                             scale, out, out_scales, residual_out, x);
+  if (st != SP_OK) return st;
+  return run_checked(cfg, partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, mode,
+                     scale, out, out_scales, residual_out, stream, x);
 }
 
 }  // namespace
@@ -353,14 +374,8 @@ sp_status sp_fused_reduce_norm(const void* partials, int tp, int64_t T_pad, int6
                                const void* bias, float eps, int quant_mode, const float* scale,
                                void* out, void* out_scales, void* residual_out,
                                sp_stream_t stream) {
-  sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode,
-                       scale, out, out_scales, residual_out);
-  if (st != SP_OK) return st;
-  sp_launch_config cfg;
-  st = sp_select_launch(tp, T_pad, H, quant_mode, &cfg);
-  if (st != SP_OK) return st;
-  return run(cfg, partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode, scale,
-             out, out_scales, residual_out, reinterpret_cast<cudaStream_t>(stream));
+  return sp_fused_reduce_norm_ex(nullptr, partials, tp, T_pad, T_valid, H, residual, weight, bias,
+                                 eps, quant_mode, scale, out, out_scales, residual_out, stream);
 }
 
 sp_status sp_fused_reduce_norm_with_config(const sp_launch_config* config, const void* partials,
@@ -397,29 +412,87 @@ static bool device_view(const void* p, const void** dev_ptr) {
   return true;
 }
 
-sp_status sp_fused_reduce_norm_host(const void* partials, int tp, int64_t T_pad, int64_t T_valid,
-                                    int64_t H, const void* residual, const void* weight,
-                                    const void* bias, float eps, int quant_mode,
-                                    const float* scale, void* out, void* out_scales,
-                                    void* residual_out, sp_stream_t stream) {
+void sp_options_init(sp_fused_options* options) {
+  if (!options) return;
+  options->partial_scale = 1.0f;
+  options->addend = nullptr;
+  options->scale_layout = SP_SCALES_ROW_MAJOR;
+  options->host_buffers = 0;
+}
+
+sp_status sp_fused_reduce_norm_ex(const sp_fused_options* options, const void* partials, int tp,
+                                  int64_t T_pad, int64_t T_valid, int64_t H, const void* residual,
+                                  const void* weight, const void* bias, float eps, int quant_mode,
+                                  const float* scale, void* out, void* out_scales,
+                                  void* residual_out, sp_stream_t stream) {
+  sp_fused_options o;
+  sp_options_init(&o);
+  if (options) o = *options;
+  Extras x;
+  x.partial_scale = o.partial_scale;
+  x.addend = o.addend;
   sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode,
-                       scale, out, out_scales, residual_out);
-  if (st != SP_OK || T_pad == 0) return st;
-  const void* host[8] = {partials, residual, weight, bias, scale, out, out_scales, residual_out};
-  const void* dev[8];
-  for (int i = 0; i < 8; ++i)
+                       scale, out, out_scales, residual_out, x);
+  if (st != SP_OK) return st;
+  if (o.scale_layout != SP_SCALES_ROW_MAJOR || (o.host_buffers != 0 && o.host_buffers != 1))
+    return SP_ERR_UNSUPPORTED;
+  if (T_pad == 0) return SP_OK;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (!o.host_buffers) {
+    sp_launch_config cfg;
+    st = sp_select_launch(tp, T_pad, H, quant_mode, &cfg);
+    if (st != SP_OK) return st;
+    return run_checked(cfg, partials, tp, T_pad, T_valid, H, residual, weight, bias, eps,
+                       quant_mode, scale, out, out_scales, residual_out, s, x);
+  }
+  // Host buffers: map every pointer to its device address and use plain 128-bit loads (the
+  // direct kernel): the host link, not HBM, bounds this call, and a few hundred KB of loads in
+  // flight per GPU cover its latency.
+  const void* host[9] = {partials, residual, weight, bias, scale, out, out_scales, residual_out,
+                         x.addend};
+  const void* dev[9];
+  for (int i = 0; i < 9; ++i)
     if (!device_view(host[i], &dev[i])) return SP_ERR_INVALID_ARG;
-  // Plain 128-bit loads (the direct kernel): the host link, not HBM, bounds this call, and a few
-  // hundred KB of loads in flight per GPU cover its latency.
   sp_launch_config cfg{};
   cfg.kernel = SP_KERNEL_DIRECT;
   cfg.vec_per_thread = consumer_threads(H, 2) > spk::kMaxConsumerThreads ? 4 : 2;
   cfg.ctas_per_sm = 4;
   cfg.stages = 0;
+  x.addend = dev[8];
   return run(cfg, dev[0], tp, T_pad, T_valid, H, dev[1], dev[2], dev[3], eps, quant_mode,
              static_cast<const float*>(dev[4]), const_cast<void*>(dev[5]),
-             const_cast<void*>(dev[6]), const_cast<void*>(dev[7]),
-             reinterpret_cast<cudaStream_t>(stream));
+             const_cast<void*>(dev[6]), const_cast<void*>(dev[7]), s, x);
+}
+
+sp_status sp_fused_reduce_norm_host(const void* partials, int tp, int64_t T_pad, int64_t T_valid,
+                                    int64_t H, const void* residual, const void* weight,
+                                    const void* bias, float eps, int quant_mode,
+                                    const float* scale, void* out, void* out_scales,
+                                    void* residual_out, sp_stream_t stream) {
+  sp_fused_options o;
+  sp_options_init(&o);
+  o.host_buffers = 1;
+  return sp_fused_reduce_norm_ex(&o, partials, tp, T_pad, T_valid, H, residual, weight, bias, eps,
+                                 quant_mode, scale, out, out_scales, residual_out, stream);
+}
+
+sp_status sp_check_args_ex(const sp_fused_options* options, const void* partials, int tp,
+                           int64_t T_pad, int64_t T_valid, int64_t H, const void* residual,
+                           const void* weight, const void* bias, float eps, int quant_mode,
+                           const float* scale, const void* out, const void* out_scales,
+                           const void* residual_out) {
+  sp_fused_options o;
+  sp_options_init(&o);
+  if (options) o = *options;
+  Extras x;
+  x.partial_scale = o.partial_scale;
+  x.addend = o.addend;
+  const sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps,
+                             quant_mode, scale, out, out_scales, residual_out, x);
+  if (st != SP_OK) return st;
+  if (o.scale_layout != SP_SCALES_ROW_MAJOR || (o.host_buffers != 0 && o.host_buffers != 1))
+    return SP_ERR_UNSUPPORTED;
+  return SP_OK;
 }
 
 sp_status sp_check_args(const void* partials, int tp, int64_t T_pad, int64_t T_valid, int64_t H,

@@ -7,8 +7,8 @@
 // Thread c of the CTA's consumer threads owns 16-byte vectors v = c + k*nthreads (k < VEC) of
 // the row, i.e. 8*VEC columns, held as fp32 accumulators in registers for the whole row.
 //
-//   k_staged  A producer thread streams the row's tp partial rows and its residual row (each a
-//             contiguous 2*H-byte segment) into a ring of shared-memory stages with bulk
+//   k_staged  A producer thread streams the row's tp partial rows, its residual row and its
+//             addend row (each a contiguous 2*H-byte segment) into a ring of stages with bulk
 //             asynchronous copies (cp.async.bulk, completion on an mbarrier per stage) while the
 //             consumer warps add the segments that have landed. The ring runs ahead across rows,
 //             so HBM stays busy through each row's reduction and epilogue, and the bytes in flight
@@ -37,9 +37,14 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
 
   const int tid = threadIdx.x;
   const int nc = p.nthreads;
-  const int nseg = p.tp + (p.residual ? 1 : 0);
+  // Row segments in stream order: partials 0 .. tp-1, then residual, then addend (if present).
+  const int nseg = p.tp + (p.residual ? 1 : 0) + (p.addend ? 1 : 0);
+  auto segment = [&](int64_t t, int seg) -> const uint16_t* {
+    if (seg < p.tp) return p.partials + seg * p.plane + t * static_cast<int64_t>(p.H);
+    if (seg == p.tp && p.residual) return p.residual + t * static_cast<int64_t>(p.H);
+    return p.addend + t * static_cast<int64_t>(p.H);
+  };
   const uint32_t seg_bytes = static_cast<uint32_t>(p.H) * 2u;
-  const int64_t H = p.H;
 
   if (tid == 0) {
     for (int s = 0; s < p.stages; ++s) {
@@ -54,8 +59,7 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
     int n = 0;
     for (int64_t t = blockIdx.x; t < p.T_valid && n < p.stages; t += gridDim.x)
       for (int seg = 0; seg < nseg && n < p.stages; ++seg, ++n)
-        bulk_prefetch_l2(seg < p.tp ? p.partials + seg * p.plane + t * H : p.residual + t * H,
-                         seg_bytes);
+        bulk_prefetch_l2(segment(t, seg), seg_bytes);
   }
   pdl_launch_dependents();
   pdl_wait_prerequisites();
@@ -71,7 +75,7 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
     bool aborted = false;
     for (int64_t t = blockIdx.x; t < p.T_valid && !aborted; t += gridDim.x) {
       for (int seg = 0; seg < nseg; ++seg) {
-        const uint16_t* src = seg < p.tp ? p.partials + seg * p.plane + t * H : p.residual + t * H;
+        const uint16_t* src = segment(t, seg);
         if (!mbar_wait_bounded(smem_addr(empty + stage), phase ^ 1u, abort_flag)) {
           if (!*static_cast<volatile int*>(abort_flag)) atomicOr(&g_error_flags, kErrWaitTimeout);
           *static_cast<volatile int*>(abort_flag) = 1;
@@ -154,6 +158,12 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
         stage = 0;
         phase ^= 1u;
       }
+      if (seg + 1 == p.tp && p.partial_scale != 1.0f) {  // the reduced partial sum is complete
+#pragma unroll
+        for (int k = 0; k < kVec; ++k)
+#pragma unroll
+          for (int e = 0; e < 8; ++e) h[k][e] *= p.partial_scale;
+      }
     }
     uint4 w[kVec];
 #pragma unroll
@@ -217,11 +227,24 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
         if (v < p.nvec) add_bf16x8(ldg_stream(row + r * p.plane + v * 8), h[k]);
       }
     }
+    if (p.partial_scale != 1.0f) {
+#pragma unroll
+      for (int k = 0; k < kVec; ++k)
+#pragma unroll
+        for (int e = 0; e < 8; ++e) h[k][e] *= p.partial_scale;
+    }
     if (p.residual) {
 #pragma unroll
       for (int k = 0; k < kVec; ++k) {
         const int v = c + k * nc;
         if (v < p.nvec) add_bf16x8(ldg_stream(p.residual + t * H + v * 8), h[k]);
+      }
+    }
+    if (p.addend) {
+#pragma unroll
+      for (int k = 0; k < kVec; ++k) {
+        const int v = c + k * nc;
+        if (v < p.nvec) add_bf16x8(ldg_stream(p.addend + t * H + v * 8), h[k]);
       }
     }
 #pragma unroll

@@ -61,12 +61,13 @@ def _normal(g: torch.Generator, shape, device) -> torch.Tensor:
 
 def make_inputs(w: dict, *, seed: int | None = None, device="cpu", T_valid: int | None = None,
                 T_pad: int | None = None, H: int | None = None, tp: int | None = None,
-                with_residual: bool = True, with_bias: bool = True,
+                with_residual: bool = True, with_bias: bool = True, with_addend: bool = False,
                 nan_padding: bool = True) -> dict:
     """Draw one problem of workload ``w`` (sizes may be overridden to shrink it).
 
     Returns a dict of tensors on ``device``: ``partials`` bf16 [tp, T_pad, H], ``residual`` bf16
-    [T_pad, H] or None, ``weight`` bf16 [H], ``bias`` bf16 [H] or None, plus the scalars
+    [T_pad, H] or None, ``weight`` bf16 [H], ``bias`` bf16 [H] or None, ``addend`` bf16
+    [T_pad, H] (0.5 N(0,1), drawn last) or None, plus the scalars
     ``tp, T_pad, T_valid, H, eps, mode, scale`` (``scale`` is a Python float or None).
     """
     tp = tp or w["tp"]
@@ -106,15 +107,19 @@ def make_inputs(w: dict, *, seed: int | None = None, device="cpu", T_valid: int 
     weight = (1.0 + 0.1 * _normal(g, (H,), device)).to(torch.bfloat16)
     bias = (0.01 * _normal(g, (H,), device)).to(torch.bfloat16) if with_bias else None
 
+    addend = (0.5 * _normal(g, (T_pad, H), device)).to(torch.bfloat16) if with_addend else None
+
     if nan_padding and T_valid < T_pad:
         partials[:, T_valid:] = float("nan")
-        if residual is not None:
-            residual[T_valid:] = float("nan")
+        for t in (residual, addend):
+            if t is not None:
+                t[T_valid:] = float("nan")
 
     scale = w.get("scale")
     if w["mode"] == "nvfp4":
         scale = nvfp4_global_scale()
-    return dict(partials=partials, residual=residual, weight=weight, bias=bias, tp=tp, T_pad=T_pad,
+    return dict(partials=partials, residual=residual, weight=weight, bias=bias, addend=addend,
+                tp=tp, T_pad=T_pad,
                 T_valid=T_valid, H=H, eps=1e-6, mode=w["mode"], scale=scale, seed=seed)
 
 

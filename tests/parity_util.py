@@ -43,11 +43,11 @@ def _pinned(t):
     return None if t is None else t.cpu().pin_memory()
 
 
-def run_gpu_host(inp: dict, *, fill: int = 0xA5, stream=None) -> dict:
+def run_gpu_host(inp: dict, *, fill: int = 0xA5, stream=None, partial_scale: float = 1.0) -> dict:
     """Run the zero-copy entry point on pinned host copies of ``inp`` into guard-banded pinned
     host outputs pre-filled with ``fill``; returns numpy results."""
     T_pad, H, mode = inp["T_pad"], inp["H"], inp["mode"]
-    hin = {k: _pinned(inp[k]) for k in ("partials", "residual", "weight", "bias")}
+    hin = {k: _pinned(inp.get(k)) for k in ("partials", "residual", "weight", "bias", "addend")}
     o_bytes = sp.sp_out_bytes(T_pad, H, mode)
     s_bytes = sp.sp_out_scales_bytes(T_pad, H, mode)
     oshape, odt, sshape, sdt = oracle.out_layout(T_pad, H, mode)
@@ -68,10 +68,18 @@ def run_gpu_host(inp: dict, *, fill: int = 0xA5, stream=None) -> dict:
     res_out = _view(res_m, (T_pad, H), torch.bfloat16)
     scale_t = (torch.tensor([inp["scale"]], dtype=torch.float32).pin_memory()
                if inp["scale"] is not None else None)
-    sp.sp_fused_reduce_norm_host(hin["partials"], hin["weight"], out, res_out,
-                                 residual=hin["residual"], bias=hin["bias"], eps=inp["eps"],
-                                 quant_mode=mode, scale=scale_t, out_scales=sc,
-                                 T_valid=inp["T_valid"], stream=stream)
+    if partial_scale == 1.0 and hin["addend"] is None:
+        sp.sp_fused_reduce_norm_host(hin["partials"], hin["weight"], out, res_out,
+                                     residual=hin["residual"], bias=hin["bias"], eps=inp["eps"],
+                                     quant_mode=mode, scale=scale_t, out_scales=sc,
+                                     T_valid=inp["T_valid"], stream=stream)
+    else:
+        opts = sp.sp_options_init(partial_scale=partial_scale, addend=hin["addend"],
+                                  host_buffers=True)
+        sp.sp_fused_reduce_norm_ex(opts, hin["partials"], hin["weight"], out, res_out,
+                                   residual=hin["residual"], bias=hin["bias"], eps=inp["eps"],
+                                   quant_mode=mode, scale=scale_t, out_scales=sc,
+                                   T_valid=inp["T_valid"], stream=stream)
     torch.cuda.synchronize()
     for w in (out_w, sc_w, res_w):
         if w is not None:
@@ -82,7 +90,7 @@ def run_gpu_host(inp: dict, *, fill: int = 0xA5, stream=None) -> dict:
 
 
 def run_gpu(inp: dict, *, config: dict | None = None, fill: int = 0xA5, inplace: bool = False,
-            stream=None) -> dict:
+            stream=None, partial_scale: float = 1.0) -> dict:
     """Run the library once on inputs ``inp`` (device tensors from synth.make_inputs) into
     guard-banded outputs pre-filled with ``fill``; returns host numpy results."""
     dev = inp["partials"].device
@@ -112,7 +120,11 @@ def run_gpu(inp: dict, *, config: dict | None = None, fill: int = 0xA5, inplace:
         scale_t = torch.tensor([inp["scale"]], dtype=torch.float32, device=dev)
     kw = dict(residual=residual, bias=inp["bias"], eps=inp["eps"], quant_mode=mode, scale=scale_t,
               out_scales=sc, T_valid=inp["T_valid"], stream=stream)
-    if config is None:
+    if partial_scale != 1.0 or inp.get("addend") is not None:
+        assert config is None
+        opts = sp.sp_options_init(partial_scale=partial_scale, addend=inp.get("addend"))
+        sp.sp_fused_reduce_norm_ex(opts, inp["partials"], inp["weight"], out, res_out, **kw)
+    elif config is None:
         sp.sp_fused_reduce_norm(inp["partials"], inp["weight"], out, res_out, **kw)
     else:
         sp.sp_fused_reduce_norm_with_config(config, inp["partials"], inp["weight"], out, res_out,
@@ -132,12 +144,14 @@ def bits_of(t: torch.Tensor) -> np.ndarray:
     return t.cpu().numpy()
 
 
-def run_oracle(inp: dict, want_y: bool = True, rows=None) -> dict:
+def run_oracle(inp: dict, want_y: bool = True, rows=None, partial_scale: float = 1.0) -> dict:
     to = synth.bf16_bits
+    add = inp.get("addend")
     res = oracle.fused_reduce_norm(
         to(inp["partials"]), None if inp["residual"] is None else to(inp["residual"]),
         to(inp["weight"]), None if inp["bias"] is None else to(inp["bias"]), inp["eps"],
-        inp["mode"], inp["scale"], inp["T_valid"], want_y=want_y, threads=CORES, rows=rows)
+        inp["mode"], inp["scale"], inp["T_valid"], want_y=want_y, threads=CORES, rows=rows,
+        partial_scale=partial_scale, addend=None if add is None else to(add))
     assert res["status"] == 0
     return res
 

@@ -168,3 +168,32 @@ def test_product_path_does_not_reference_the_oracle():
             src = open(path).read()
             assert "import oracle" not in src and "from oracle" not in src, path
             assert "sp_oracle" not in src and "libsporacle" not in src, path
+
+
+OPTION_CASES = [
+    (dict(), {}, "SP_OK"),
+    (dict(partial_scale=0.5), {}, "SP_OK"),
+    (dict(partial_scale=float("inf")), {}, "SP_ERR_INVALID_ARG"),
+    (dict(partial_scale=float("nan")), {}, "SP_ERR_INVALID_ARG"),
+    (dict(addend=A * 20), {}, "SP_OK"),
+    (dict(addend=A * 20 + 8), {}, "SP_ERR_ALIGNMENT"),
+    (dict(addend=A * 11 + 64), {}, "SP_ERR_INVALID_ARG"),          # inside `out`
+    (dict(addend=A * 13), {}, "SP_ERR_INVALID_ARG"),                # is residual_out
+    (dict(scale_layout=1), {}, "SP_ERR_UNSUPPORTED"),
+    (dict(host_buffers=2), {}, "SP_ERR_UNSUPPORTED"),
+    (dict(addend=A * 20), {"T_pad": 18}, "SP_ERR_INVALID_ARG"),     # shape rule first
+]
+
+
+@pytest.mark.parametrize("opt,kw,want", OPTION_CASES)
+def test_option_checks(lib, opt, kw, want):
+    o = sp.Options()
+    lib.sp_options_init(ctypes.byref(o))
+    assert o.partial_scale == 1.0 and o.addend is None and o.scale_layout == 0
+    for k, v in opt.items():
+        setattr(o, k, v)
+    a = {**_base(), **kw}
+    st = sp.sp_check_args_ex(o, a["partials"], a["tp"], a["T_pad"], a["T_valid"], a["H"],
+                             a["residual"], a["weight"], a["bias"], a["eps"], a["quant_mode"],
+                             a["scale"], a["out"], a["out_scales"], a["residual_out"])
+    assert sp.sp_status_string(st) == want

@@ -168,5 +168,23 @@ def test_host_entry_rejects_pageable_memory():
     assert e.value.status == 1
 
 
+@pytest.mark.parametrize("mode", ["none", "fp8_static", "fp8_per_token", "nvfp4"])
+@pytest.mark.parametrize("c,with_addend,with_residual", [(0.5, True, True), (1.0 / 3.0, False, True),
+                                                         (-1.25, True, False), (1.0, True, True)])
+@pytest.mark.parametrize("host", [False, True])
+def test_partial_scale_and_addend(mode, c, with_addend, with_residual, host):
+    """sp_fused_reduce_norm_ex: h = c * sum_r p_r + bias + residual + addend."""
+    w = dict(synth.workload(3), mode=mode, scale=0.05 if mode == "fp8_static" else None)
+    inp = synth.make_inputs(w, device=DEV, T_pad=336, T_valid=331, H=5120,
+                            with_addend=with_addend, with_residual=with_residual)
+    run = run_gpu_host if host else run_gpu
+    a = run(inp, fill=0xA5, partial_scale=c)
+    b = run(inp, fill=0x5A, partial_scale=c)
+    for k in ("out", "out_scales", "residual_out"):
+        if a[k] is not None:
+            assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+    compare(a, run_oracle(inp, partial_scale=c), inp)
+
+
 def test_no_device_wait_ran_out():
     assert sp.sp_device_error(clear=False) == 0
