@@ -157,7 +157,13 @@ VARIANTS = {
     "first": dict(with_residual=False),
     # a scale on every partial before the reduction plus a per-shard addend after it
     "scaled_addend": dict(with_addend=True, partial_scale=0.5),
+    # NVFP4 block scales written in the 128x4-tile layout block-scaled GEMMs read
+    "swizzled_scales": dict(scale_layout=1),
 }
+# (workload, variant) pairs measured beside the other workloads
+VARIANT_RUNS = [("tp4_T4093p4096_H4096_bf16", "first"),
+                ("tp4_T4093p4096_H4096_bf16", "scaled_addend"),
+                ("tp8_T16384_H5120_nvfp4", "swizzled_scales")]
 
 
 class Problem:
@@ -167,9 +173,11 @@ class Problem:
         from sequence_reduce_add_gb300 import synth
         v = dict(VARIANTS.get(variant, {}))
         partial_scale = v.pop("partial_scale", 1.0)
+        scale_layout = v.pop("scale_layout", 0)
         self.inp = synth.make_inputs(w, seed=seed, device=device, **v)
         i = self.inp
-        self.outs = sp.allocate_outputs(i["T_pad"], i["H"], i["mode"], device)
+        self.outs = sp.allocate_outputs(i["T_pad"], i["H"], i["mode"], device,
+                                        scale_layout=scale_layout)
         self.scale = (torch.tensor([i["scale"]], dtype=torch.float32, device=device)
                       if i["scale"] is not None else None)
         p = lambda t: None if t is None else t.data_ptr()  # noqa: E731
@@ -179,7 +187,8 @@ class Problem:
                      p(self.outs["out_scales"]), p(self.outs["residual_out"]))
         self.fn_name = "sp_fused_reduce_norm"
         if variant is not None:  # the options entry point
-            self.options = sp.sp_options_init(partial_scale=partial_scale, addend=i["addend"])
+            self.options = sp.sp_options_init(partial_scale=partial_scale, addend=i["addend"],
+                                              scale_layout=scale_layout)
             self.args = (ctypes.byref(self.options),) + self.args
             self.fn_name = "sp_fused_reduce_norm_ex"
         self.bytes = algorithmic_bytes(i["tp"], i["T_valid"], i["T_pad"], i["H"], i["mode"],
@@ -416,9 +425,9 @@ def run_ours(args) -> None:
             if other["name"] == w["name"]:
                 continue
             extras[other["name"]] = bench_extra(lib, sp, synth, other, device, stream, peak)
-        for variant in VARIANTS:
-            extras[f"{w['name']}+{variant}"] = bench_extra(lib, sp, synth, w, device, stream,
-                                                           peak, variant)
+        for name, variant in VARIANT_RUNS:
+            extras[f"{name}+{variant}"] = bench_extra(lib, sp, synth, synth.workload(name),
+                                                      device, stream, peak, variant)
 
     if rank != 0:
         return
@@ -464,8 +473,8 @@ def bench_extra(lib, sp, synth, w, device, stream, peak, variant: str | None = N
     problems = [base] + [Problem(w, base.inp["seed"] + 1000 * k, device, sp, variant)
                          for k in range(1, sets)]
     one = base.bytes
-    steps = max(20, int(0.25e9 / max(one, 1)) * 4)
-    steps = min(steps, 4000)
+    # about 50 ms of timed launches at ~6.5 TB/s (at least 20, at most 4000 launches)
+    steps = int(min(4000, max(20, 0.05 * 6.5e12 / max(one, 1))))
     time_kernel_loop(lib, problems, 10, stream, False)
     total, _ = time_kernel_loop(lib, problems, steps, stream, False)
     _, launches = time_kernel_loop(lib, problems, min(steps, 100), stream, True)

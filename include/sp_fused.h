@@ -135,12 +135,18 @@ sp_status sp_check_args(const void* partials, int tp, int64_t T_pad, int64_t T_v
  *                  part of the new residual: h = partial_scale * sum_r partials[r][t] + bias +
  *                  residual[t] + addend[t] (the per-shard extra input of the Qwen3-VL deepstack
  *                  rewrite, vllm-ascend SP notes §2.3); NULL = none. Never read on padding rows.
- *   scale_layout   NVFP4 block scales: SP_SCALES_ROW_MAJOR ([T_pad][H/16]); other values are
- *                  SP_ERR_UNSUPPORTED.
+ *   scale_layout   NVFP4 block scales: SP_SCALES_ROW_MAJOR ([T_pad][H/16], one byte per block)
+ *                  or SP_SCALES_SWIZZLED_128X4, the layout block-scaled GEMMs read: the
+ *                  [T_pad][H/16] scale matrix padded to R = ceil(T_pad/128)*128 rows and
+ *                  C = ceil(H/64)*4 columns (padding bytes written as zero), stored as 512-byte
+ *                  tiles of 128 rows x 4 columns, tile (i, j) at byte (i * C/4 + j) * 512 and row r,
+ *                  column c of a tile at (r % 32) * 16 + (r / 32) * 4 + c; out_scales then holds
+ *                  R * C bytes (sp_out_scales_bytes_ex). SWIZZLED with another mode is
+ *                  SP_ERR_INVALID_ARG; any other value SP_ERR_UNSUPPORTED.
  *   host_buffers   0: every tensor is in device memory; 1: tensors are in page-locked host memory
  *                  (or device memory) and are read/written across the host link (zero-copy).
  */
-enum { SP_SCALES_ROW_MAJOR = 0 };
+enum { SP_SCALES_ROW_MAJOR = 0, SP_SCALES_SWIZZLED_128X4 = 1 };
 
 typedef struct sp_fused_options {
   float partial_scale;
@@ -228,8 +234,8 @@ sp_status sp_fused_reduce_norm_with_config(const sp_launch_config* config /* hos
  *   sp_shard_rows: rows [*start, *start + *len) of shard `rank` — the contiguous segment of
  *       T_pad/tp rows that rank owns (PR #18671 notes §2, §5.2); SP_ERR_INVALID_ARG when
  *       T_pad % tp != 0 or rank is out of range.
- *   sp_out_bytes / sp_out_scales_bytes: sizes of `out` and `out_scales` for a mode (0 for no
- *       buffer), or -1 for an invalid mode.
+ *   sp_out_bytes / sp_out_scales_bytes(_ex): sizes of `out` and `out_scales` for a mode (and a
+ *       scale layout; 0 for no buffer), or -1 for an invalid mode or layout.
  *   sp_max_hidden: the largest H the kernels take.
  */
 int64_t sp_pad_tokens(int64_t T, int tp);
@@ -237,6 +243,7 @@ sp_status sp_shard_rows(int64_t T_pad, int tp, int rank, int64_t* start /* host 
                         int64_t* len /* host */);
 int64_t sp_out_bytes(int64_t T_pad, int64_t H, int quant_mode);
 int64_t sp_out_scales_bytes(int64_t T_pad, int64_t H, int quant_mode);
+int64_t sp_out_scales_bytes_ex(int64_t T_pad, int64_t H, int quant_mode, int scale_layout);
 int64_t sp_max_hidden(void);
 
 /* Name of a status code, e.g. "SP_ERR_ALIGNMENT"; "SP_UNKNOWN_STATUS" for other values. */

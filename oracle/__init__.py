@@ -48,7 +48,9 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.sp_oracle_fused_reduce_norm_rows.argtypes = _ARGS + [_f64p, _i64, _i64]
     lib.sp_oracle_fused_reduce_norm_rows.restype = ctypes.c_int
     lib.sp_oracle_fused_reduce_norm_rows_ex.argtypes = _ARGS + [_f64p, _i64, _i64, ctypes.c_float,
-                                                                 _u16p]
+                                                                 _u16p, ctypes.c_int]
+    lib.sp_oracle_out_scales_bytes.argtypes = [_i64, _i64, ctypes.c_int, ctypes.c_int]
+    lib.sp_oracle_out_scales_bytes.restype = _i64
     lib.sp_oracle_fused_reduce_norm_rows_ex.restype = ctypes.c_int
     for name, cin, cout in (("bf16_encode", _f64p, _u16p), ("bf16_decode", _u16p, _f64p),
                             ("e4m3_encode", _f64p, _u8p), ("e4m3_decode", _u8p, _f64p),
@@ -67,8 +69,12 @@ def _ptr(a: np.ndarray | None, ctype):
     return a.ctypes.data_as(ctypes.POINTER(ctype))
 
 
-def out_layout(T_pad: int, H: int, mode: str):
-    """(out shape, out dtype, scales shape or None, scales dtype or None) for a mode."""
+def out_layout(T_pad: int, H: int, mode: str, scale_layout: int = 0):
+    """(out shape, out dtype, scales shape or None, scales dtype or None) for a mode (the
+    swizzled NVFP4 scale layout is a flat byte buffer)."""
+    if mode == "nvfp4" and scale_layout == 1:
+        n = -(-T_pad // 128) * 128 * (-(-(H // 16) // 4) * 4)
+        return (T_pad, H // 2), np.uint8, (n,), np.uint8
     if mode == "none":
         return (T_pad, H), np.uint16, None, None
     if mode == "fp8_static":
@@ -85,7 +91,7 @@ def fused_reduce_norm(partials: np.ndarray, residual: np.ndarray | None, weight:
                       T_valid: int, *, want_y: bool = False, rows: tuple[int, int] | None = None,
                       threads: int = 1, lib: ctypes.CDLL | None = None,
                       buffers: dict | None = None, partial_scale: float = 1.0,
-                      addend: np.ndarray | None = None) -> dict:
+                      addend: np.ndarray | None = None, scale_layout: int = 0) -> dict:
     """Run the oracle over rows ``rows`` (default all) of a [tp, T_pad, H] problem.
 
     Returns a dict with ``status``, ``out``, ``out_scales`` (or None), ``residual_out`` and, when
@@ -96,7 +102,7 @@ def fused_reduce_norm(partials: np.ndarray, residual: np.ndarray | None, weight:
     """
     lib = lib or load()
     tp, T_pad, H = partials.shape
-    oshape, odt, sshape, sdt = out_layout(T_pad, H, mode)
+    oshape, odt, sshape, sdt = out_layout(T_pad, H, mode, scale_layout)
     if buffers is not None:
         out, out_scales = buffers["out"], buffers["out_scales"]
         residual_out, y = buffers["residual_out"], buffers["y"] if want_y else None
@@ -117,13 +123,13 @@ def fused_reduce_norm(partials: np.ndarray, residual: np.ndarray | None, weight:
     begin, end = rows if rows is not None else (0, T_pad)
     status = [0]
 
-    extended = partial_scale != 1.0 or addend is not None
+    extended = partial_scale != 1.0 or addend is not None or scale_layout != 0
 
     def run(b, e, slot):
         if extended:
             st = lib.sp_oracle_fused_reduce_norm_rows_ex(
                 *args, _ptr(y, ctypes.c_double), b, e, ctypes.c_float(partial_scale),
-                _ptr(addend, ctypes.c_uint16))
+                _ptr(addend, ctypes.c_uint16), scale_layout)
         else:
             st = lib.sp_oracle_fused_reduce_norm_rows(*args, _ptr(y, ctypes.c_double), b, e)
         if st != 0:

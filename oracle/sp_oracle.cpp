@@ -150,6 +150,7 @@ double as_fp32(double v) { return static_cast<double>(static_cast<float>(v)); }
 struct Args {
   float partial_scale;        // multiplies every partial before the reduction (1 = none)
   const uint16_t* addend;     // bf16 [T_pad][H] added after the reduction, or null
+  int scale_layout;           // NVFP4 block scales: 0 row-major, 1 128x4-tile swizzle
   const uint16_t* partials;
   int tp;
   int64_t T_pad;
@@ -176,9 +177,28 @@ int64_t out_bytes(const Args& a) {
   }
 }
 
+// The 128x4-tile layout of NVFP4 block scales that block-scaled GEMMs read (cuBLAS "1D block
+// scaling factors" layout): the [rows][cols] scale matrix is padded to multiples of 128 rows and
+// 4 columns; tile (i, j) = rows 128i.., columns 4j.. is a 512-byte block at (i * tiles_per_row + j)
+// * 512; inside it, row r and column c sit at (r % 32) * 16 + (r / 32) * 4 + c.
+// On the CPU this map is pinned only by the permutation property (every row-major scale once,
+// padding zero); a GPU test pins the placement itself by feeding the library's output, whose
+// parity with this function is tested, to cuBLASLt's block-scaled NVFP4 GEMM.
+int64_t swizzled_rows(int64_t T_pad) { return (T_pad + 127) / 128 * 128; }
+int64_t swizzled_cols(int64_t H) { return (H / 16 + 3) / 4 * 4; }
+int64_t swizzled_offset(int64_t row, int64_t col, int64_t H) {
+  const int64_t tiles_per_row = swizzled_cols(H) / 4;
+  const int64_t tile = (row / 128) * tiles_per_row + col / 4;
+  const int64_t r = row % 128, c = col % 4;
+  return tile * 512 + (r % 32) * 16 + (r / 32) * 4 + c;
+}
+
 int64_t scale_bytes(const Args& a) {
   if (a.mode == kFp8PerToken) return a.T_pad * 4;
-  if (a.mode == kNvfp4) return a.T_pad * (a.H / 16);
+  if (a.mode == kNvfp4) {
+    if (a.scale_layout == 1) return swizzled_rows(a.T_pad) * swizzled_cols(a.H);
+    return a.T_pad * (a.H / 16);
+  }
   return 0;
 }
 
@@ -203,6 +223,8 @@ int validate(const Args& a) {
   // Outputs must not overlap any input or each other; residual_out may be residual itself.
   const int64_t rows = a.T_pad * a.H * 2;
   if (!std::isfinite(a.partial_scale)) return kInvalidArg;
+  if (a.scale_layout != 0 && a.scale_layout != 1) return kUnsupported;
+  if (a.scale_layout == 1 && a.mode != kNvfp4) return kInvalidArg;
   const void* inputs[] = {a.partials, a.residual, a.weight, a.bias, a.scale, a.addend};
   const int64_t in_n[] = {rows * a.tp, rows, a.H * 2, a.H * 2, 4, rows};
   const void* outputs[] = {a.out, a.out_scales, a.residual_out};
@@ -229,6 +251,12 @@ int validate(const Args& a) {
 // o_proj paragraph; [SP/FC] §3.3). On one device the scatter/gather are pure indexing: row t of
 // the output is row t of the AllGather result ([SP/FC] §2.2 conclusion 1).
 // ---------------------------------------------------------------------------------------------
+// Where block scale (row t, block b) is stored.
+uint8_t* scale_slot(const Args& a, int64_t t, int64_t b) {
+  uint8_t* base = static_cast<uint8_t*>(a.out_scales);
+  return a.scale_layout == 1 ? base + swizzled_offset(t, b, a.H) : base + t * (a.H / 16) + b;
+}
+
 void zero_row(const Args& a, int64_t t, double* y_out) {
   const int64_t H = a.H;
   std::memset(a.residual_out + t * H, 0, static_cast<size_t>(H) * 2);
@@ -242,7 +270,7 @@ void zero_row(const Args& a, int64_t t, double* y_out) {
       break;
     case kNvfp4:
       std::memset(out + t * (H / 2), 0, static_cast<size_t>(H / 2));
-      std::memset(static_cast<uint8_t*>(a.out_scales) + t * (H / 16), 0, static_cast<size_t>(H / 16));
+      for (int64_t b = 0; b < H / 16; ++b) *scale_slot(a, t, b) = 0;
       break;
   }
   if (y_out) std::fill(y_out + t * H, y_out + (t + 1) * H, 0.0);
@@ -304,14 +332,13 @@ void one_row(const Args& a, int64_t t, double* y_out) {
     // per-block: 16-element blocks along H never cross a row, hence never a rank
     // ([SP-Q] §四 table, row 4)
     const double gs = static_cast<double>(*a.scale);
-    uint8_t* sf_row = static_cast<uint8_t*>(a.out_scales) + t * (H / 16);
     uint8_t* q_row = out8 + t * (H / 2);
     for (int64_t b = 0; b < H / 16; ++b) {
       double amax = 0.0;
       for (int64_t j = 16 * b; j < 16 * b + 16; ++j) amax = std::max(amax, std::fabs(y[j]));
       const uint8_t sf = e4m3_code(as_fp32(gs * amax / 6.0));
       const double sf_value = decode_bits(sf, kE4M3);
-      sf_row[b] = sf;
+      *scale_slot(a, t, b) = sf;
       for (int64_t j = 16 * b; j < 16 * b + 16; j += 2) {
         const uint8_t lo = sf_value == 0.0 ? 0 : e2m1_code(as_fp32(y[j] * gs / sf_value));
         const uint8_t hi = sf_value == 0.0 ? 0 : e2m1_code(as_fp32(y[j + 1] * gs / sf_value));
@@ -324,9 +351,20 @@ void one_row(const Args& a, int64_t t, double* y_out) {
 Args make_args(const uint16_t* partials, int tp, int64_t T_pad, int64_t T_valid, int64_t H,
                const uint16_t* residual, const uint16_t* weight, const uint16_t* bias, float eps,
                int mode, const float* scale, void* out, void* out_scales, uint16_t* residual_out,
-               float partial_scale = 1.0f, const uint16_t* addend = nullptr) {
-  return Args{partial_scale, addend, partials, tp, T_pad, T_valid, H, residual, weight, bias, eps,
-              mode, scale, out, out_scales, residual_out};
+               float partial_scale = 1.0f, const uint16_t* addend = nullptr,
+               int scale_layout = 0) {
+  return Args{partial_scale, addend, scale_layout, partials, tp, T_pad, T_valid, H, residual,
+              weight, bias, eps, mode, scale, out, out_scales, residual_out};
+}
+
+// Swizzled layout: every padding byte of the scale matrix (rows T_pad .. padded rows, columns
+// H/16 .. padded columns) is zero.
+void zero_scale_padding(const Args& a) {
+  if (a.mode != kNvfp4 || a.scale_layout != 1) return;
+  uint8_t* base = static_cast<uint8_t*>(a.out_scales);
+  for (int64_t t = 0; t < swizzled_rows(a.T_pad); ++t)
+    for (int64_t b = 0; b < swizzled_cols(a.H); ++b)
+      if (t >= a.T_pad || b >= a.H / 16) base[swizzled_offset(t, b, a.H)] = 0;
 }
 
 }  // namespace
@@ -372,14 +410,26 @@ int sp_oracle_fused_reduce_norm_rows_ex(const uint16_t* partials, int tp, int64_
                                         int quant_mode, const float* scale, void* out,
                                         void* out_scales, uint16_t* residual_out, double* y_out,
                                         int64_t row_begin, int64_t row_end, float partial_scale,
-                                        const uint16_t* addend) {
+                                        const uint16_t* addend, int scale_layout) {
   const Args a = make_args(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode,
-                           scale, out, out_scales, residual_out, partial_scale, addend);
+                           scale, out, out_scales, residual_out, partial_scale, addend,
+                           scale_layout);
   const int st = validate(a);
   if (st != kOk) return st;
   if (row_begin < 0 || row_end > T_pad || row_begin > row_end) return kInvalidArg;
+  if (row_begin == 0) zero_scale_padding(a);
   for (int64_t t = row_begin; t < row_end; ++t) one_row(a, t, y_out);
   return kOk;
+}
+
+// Size in bytes of out_scales for a mode and scale layout.
+int64_t sp_oracle_out_scales_bytes(int64_t T_pad, int64_t H, int quant_mode, int scale_layout) {
+  Args a{};
+  a.T_pad = T_pad;
+  a.H = H;
+  a.mode = quant_mode;
+  a.scale_layout = scale_layout;
+  return scale_bytes(a);
 }
 
 // Argument rules alone.

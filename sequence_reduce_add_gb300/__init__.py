@@ -23,7 +23,7 @@ __all__ = [
     "sp_fused_reduce_norm_with_config", "sp_check_args", "sp_select_launch", "sp_pad_tokens",
     "sp_shard_rows", "sp_out_bytes", "sp_out_scales_bytes", "sp_max_hidden", "sp_status_string",
     "sp_device_error", "allocate_outputs", "LaunchConfig", "Options", "sp_options_init",
-    "sp_fused_reduce_norm_ex", "sp_check_args_ex",
+    "sp_fused_reduce_norm_ex", "sp_check_args_ex", "sp_out_scales_bytes_ex",
 ]
 
 QUANT_MODES = {"none": 0, "fp8_static": 1, "fp8_per_token": 2, "nvfp4": 3,
@@ -106,6 +106,8 @@ def load_library() -> ctypes.CDLL:
     lib.sp_out_bytes.restype = _i64
     lib.sp_out_scales_bytes.argtypes = [_i64, _i64, ctypes.c_int]
     lib.sp_out_scales_bytes.restype = _i64
+    lib.sp_out_scales_bytes_ex.argtypes = [_i64, _i64, ctypes.c_int, ctypes.c_int]
+    lib.sp_out_scales_bytes_ex.restype = _i64
     lib.sp_max_hidden.argtypes = []
     lib.sp_max_hidden.restype = _i64
     lib.sp_status_string.argtypes = [ctypes.c_int]
@@ -259,6 +261,10 @@ def sp_out_scales_bytes(T_pad: int, H: int, quant_mode) -> int:
     return load_library().sp_out_scales_bytes(T_pad, H, _mode(quant_mode))
 
 
+def sp_out_scales_bytes_ex(T_pad: int, H: int, quant_mode, scale_layout: int) -> int:
+    return load_library().sp_out_scales_bytes_ex(T_pad, H, _mode(quant_mode), scale_layout)
+
+
 def sp_max_hidden() -> int:
     return load_library().sp_max_hidden()
 
@@ -275,9 +281,11 @@ def sp_device_error(clear: bool = True) -> int:
     return flags.value
 
 
-def allocate_outputs(T_pad: int, H: int, quant_mode, device, residual_out: bool = True) -> dict:
+def allocate_outputs(T_pad: int, H: int, quant_mode, device, residual_out: bool = True,
+                     scale_layout: int = 0) -> dict:
     """Uninitialised output tensors for a call: ``out``, ``out_scales`` (or None) and
-    ``residual_out`` (the kernel writes every byte of each)."""
+    ``residual_out`` (the kernel writes every byte of each). With the swizzled NVFP4 scale
+    layout ``out_scales`` is a flat uint8 buffer of sp_out_scales_bytes_ex bytes."""
     import torch
     mode = _mode(quant_mode)
     if mode == 0:
@@ -291,6 +299,9 @@ def allocate_outputs(T_pad: int, H: int, quant_mode, device, residual_out: bool 
     scales = None
     if mode == 2:
         scales = torch.empty((T_pad,), dtype=torch.float32, device=device)
+    elif mode == 3 and scale_layout == 1:
+        scales = torch.empty((sp_out_scales_bytes_ex(T_pad, H, mode, 1),), dtype=torch.uint8,
+                             device=device)
     elif mode == 3:
         scales = torch.empty((T_pad, H // 16), dtype=torch.uint8, device=device)
     res = torch.empty((T_pad, H), dtype=torch.bfloat16, device=device) if residual_out else None

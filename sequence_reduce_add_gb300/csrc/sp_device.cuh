@@ -25,6 +25,9 @@ struct Params {
   const uint16_t* residual;   // bf16 [T_pad][H] or null
   const uint16_t* addend;     // bf16 [T_pad][H] or null: added after the reduction
   float partial_scale;        // multiplies the sum of the partials (1 = none)
+  int scale_swizzled;         // NVFP4 block scales in the 128x4-tile layout (else row-major)
+  int sf_cols;                // swizzled layout: block columns padded to a multiple of 4
+  int64_t rows_total;         // rows the CTAs walk: T_pad, or the 128-padded scale rows if more
   const uint16_t* weight;     // bf16 [H]
   const uint16_t* bias;       // bf16 [H] or null
   const float* scale;         // fp32 [1] or null
@@ -322,25 +325,54 @@ __device__ __forceinline__ QuantConst load_quant_const(const Params& p) {
   return q;
 }
 
-// Zero every output byte of padding row t that this thread owns.
+// Byte offset of NVFP4 block scale (row t, block b): row-major [T_pad][H/16], or the 128x4-tile
+// layout block-scaled GEMMs read (scale matrix padded to 128 rows x 4 columns; tile (i, j) is a
+// 512-byte block at (i * sf_cols/4 + j) * 512, row r / column c of it at (r%32)*16 + (r/32)*4 + c).
+// Split as a per-row base (computed once per row) plus a per-block column offset.
+__device__ __forceinline__ int64_t scale_row_base(const Params& p, int64_t t) {
+  if (!p.scale_swizzled) return t * (p.H / 16);
+  const int r = static_cast<int>(t & 127);
+  return (t >> 7) * static_cast<int64_t>(p.sf_cols) * 128 + (r & 31) * 16 + (r >> 5) * 4;
+}
+__device__ __forceinline__ int scale_col_offset(const Params& p, int b) {
+  return p.scale_swizzled ? (b >> 2) * 512 + (b & 3) : b;
+}
+__device__ __forceinline__ int64_t scale_offset(const Params& p, int64_t t, int b) {
+  return scale_row_base(p, t) + scale_col_offset(p, b);
+}
+
+// Swizzled layout: the padding columns H/16 .. sf_cols of a row (at most 3) are zero. Block
+// column b pairs with vectors 2b, 2b+1; the thread that owns vector v = 2b (v >= nvec for a
+// padding column) writes the zero. Threads cover nthreads*VEC >= nvec rounded up to 32*VEC
+// vectors, which reaches 2*sf_cols (nvec rounded up to 8).
+__device__ __forceinline__ bool is_scale_pad_vector(const Params& p, int v) {
+  return p.scale_swizzled && v >= p.nvec && (v & 1) == 0 && v < 2 * p.sf_cols;
+}
+
+// Zero every output byte of padding row t that this thread owns. Rows at or beyond T_pad exist
+// only in the swizzled NVFP4 scale layout (rows padded to 128): there only the scales are written.
 template <int kVec, int kMode>
 __device__ __forceinline__ void zero_row(const Params& p, int64_t t, int c) {
   const int64_t H = p.H;
+  const bool real_row = t < p.T_pad;
 #pragma unroll
   for (int k = 0; k < kVec; ++k) {
     const int v = c + k * p.nthreads;
+    if (kMode == kModeNvfp4 && is_scale_pad_vector(p, v))
+      static_cast<uint8_t*>(p.out_scales)[scale_offset(p, t, v / 2)] = 0;
     if (v >= p.nvec) continue;
-    stg_stream(p.residual_out + t * H + v * 8, make_uint4(0, 0, 0, 0));
+    if (real_row) stg_stream(p.residual_out + t * H + v * 8, make_uint4(0, 0, 0, 0));
+    if (kMode != kModeNvfp4 && !real_row) continue;
     if (kMode == kModeNone) {
       stg_stream(static_cast<uint16_t*>(p.out) + t * H + v * 8, make_uint4(0, 0, 0, 0));
     } else if (kMode == kModeFp8Static || kMode == kModeFp8PerToken) {
       stg_stream(static_cast<uint8_t*>(p.out) + t * H + v * 8, make_uint2(0, 0));
     } else {
-      stg_stream(static_cast<uint8_t*>(p.out) + t * (H / 2) + v * 4, 0u);
-      if ((v & 1) == 0) static_cast<uint8_t*>(p.out_scales)[t * (H / 16) + v / 2] = 0;
+      if (real_row) stg_stream(static_cast<uint8_t*>(p.out) + t * (H / 2) + v * 4, 0u);
+      if ((v & 1) == 0) static_cast<uint8_t*>(p.out_scales)[scale_offset(p, t, v / 2)] = 0;
     }
   }
-  if (kMode == kModeFp8PerToken && c == 0) static_cast<float*>(p.out_scales)[t] = 0.0f;
+  if (kMode == kModeFp8PerToken && c == 0 && real_row) static_cast<float*>(p.out_scales)[t] = 0.0f;
 }
 
 // Finish row t: h holds sum_r partials + residual + bias for this thread's vectors (zero for
@@ -418,6 +450,7 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
                               pack_e4m3x4(q[4], q[5], q[6], q[7])));
     }
   } else {  // NVFP4: 16-element blocks = vectors (2m, 2m+1), held by lanes (c, c^1)
+    uint8_t* sf_row = static_cast<uint8_t*>(p.out_scales) + scale_row_base(p, t);
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
       const int v = c + k * p.nthreads;
@@ -436,8 +469,9 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
       for (int e = 0; e < 8; ++e) y[e] *= mult;
       if (v < p.nvec) {
         stg_stream(static_cast<uint8_t*>(p.out) + t * (H / 2) + v * 4, pack_e2m1x8(y));
-        if ((v & 1) == 0) static_cast<uint8_t*>(p.out_scales)[t * (H / 16) + v / 2] =
-            static_cast<uint8_t>(sf);
+        if ((v & 1) == 0) sf_row[scale_col_offset(p, v >> 1)] = static_cast<uint8_t>(sf);
+      } else if (is_scale_pad_vector(p, v)) {
+        sf_row[scale_col_offset(p, v >> 1)] = 0;
       }
     }
   }

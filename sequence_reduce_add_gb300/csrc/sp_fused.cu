@@ -25,12 +25,19 @@ int64_t out_bytes_of(int64_t T_pad, int64_t H, int mode) {
   }
 }
 
-int64_t scale_bytes_of(int64_t T_pad, int64_t H, int mode) {
+int64_t swizzled_scale_rows(int64_t T_pad) { return (T_pad + 127) / 128 * 128; }
+int64_t swizzled_scale_cols(int64_t H) { return (H / 16 + 3) / 4 * 4; }
+
+int64_t scale_bytes_of(int64_t T_pad, int64_t H, int mode, int layout = SP_SCALES_ROW_MAJOR) {
+  if (layout != SP_SCALES_ROW_MAJOR && layout != SP_SCALES_SWIZZLED_128X4) return -1;
+  if (layout == SP_SCALES_SWIZZLED_128X4 && mode != SP_QUANT_NVFP4) return -1;
   switch (mode) {
     case SP_QUANT_NONE:
     case SP_QUANT_FP8_STATIC: return 0;
     case SP_QUANT_FP8_PER_TOKEN: return T_pad * 4;
-    case SP_QUANT_NVFP4: return T_pad * (H / 16);
+    case SP_QUANT_NVFP4:
+      return layout == SP_SCALES_SWIZZLED_128X4 ? swizzled_scale_rows(T_pad) * swizzled_scale_cols(H)
+                                                : T_pad * (H / 16);
     default: return -1;
   }
 }
@@ -50,6 +57,7 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 struct Extras {
   float partial_scale = 1.0f;
   const void* addend = nullptr;
+  int scale_layout = SP_SCALES_ROW_MAJOR;
 };
 
 sp_status check(const void* partials, int tp, int64_t T_pad, int64_t T_valid, int64_t H,
@@ -64,6 +72,9 @@ sp_status check(const void* partials, int tp, int64_t T_pad, int64_t T_valid, in
   if (mode == SP_QUANT_NVFP4 && H % 16 != 0) return SP_ERR_INVALID_ARG;
   if (!(eps > 0.0f) || !std::isfinite(eps)) return SP_ERR_INVALID_ARG;
   if (!std::isfinite(x.partial_scale)) return SP_ERR_INVALID_ARG;
+  if (x.scale_layout != SP_SCALES_ROW_MAJOR && x.scale_layout != SP_SCALES_SWIZZLED_128X4)
+    return SP_ERR_UNSUPPORTED;
+  if (x.scale_layout == SP_SCALES_SWIZZLED_128X4 && mode != SP_QUANT_NVFP4) return SP_ERR_INVALID_ARG;
   if (T_pad == 0) return SP_OK;
   if (!partials || !weight || !out || !residual_out) return SP_ERR_INVALID_ARG;
   if ((mode == SP_QUANT_FP8_STATIC || mode == SP_QUANT_NVFP4) && !scale) return SP_ERR_INVALID_ARG;
@@ -73,7 +84,8 @@ sp_status check(const void* partials, int tp, int64_t T_pad, int64_t T_valid, in
   const void* inputs[] = {partials, residual, weight, bias, scale, x.addend};
   const int64_t in_n[] = {rows * tp, rows, H * 2, H * 2, 4, rows};
   const void* outputs[] = {out, out_scales, residual_out};
-  const int64_t out_n[] = {out_bytes_of(T_pad, H, mode), scale_bytes_of(T_pad, H, mode), rows};
+  const int64_t out_n[] = {out_bytes_of(T_pad, H, mode),
+                           scale_bytes_of(T_pad, H, mode, x.scale_layout), rows};
   for (int o = 0; o < 3; ++o) {
     for (int i = 0; i < 6; ++i) {
       if (o == 2 && i == 1 && residual_out == residual) continue;  // in-place residual update
@@ -294,6 +306,9 @@ sp_status run_checked(const sp_launch_config& cfg_in, const void* partials, int 
   p.residual = static_cast<const uint16_t*>(residual);
   p.addend = static_cast<const uint16_t*>(x.addend);
   p.partial_scale = x.partial_scale;
+  p.scale_swizzled = x.scale_layout == SP_SCALES_SWIZZLED_128X4 ? 1 : 0;
+  p.sf_cols = static_cast<int>(swizzled_scale_cols(H));
+  p.rows_total = p.scale_swizzled ? swizzled_scale_rows(T_pad) : T_pad;
   p.weight = static_cast<const uint16_t*>(weight);
   p.bias = static_cast<const uint16_t*>(bias);
   p.scale = scale;
@@ -431,11 +446,11 @@ sp_status sp_fused_reduce_norm_ex(const sp_fused_options* options, const void* p
   Extras x;
   x.partial_scale = o.partial_scale;
   x.addend = o.addend;
+  x.scale_layout = o.scale_layout;
   sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode,
                        scale, out, out_scales, residual_out, x);
   if (st != SP_OK) return st;
-  if (o.scale_layout != SP_SCALES_ROW_MAJOR || (o.host_buffers != 0 && o.host_buffers != 1))
-    return SP_ERR_UNSUPPORTED;
+  if (o.host_buffers != 0 && o.host_buffers != 1) return SP_ERR_UNSUPPORTED;
   if (T_pad == 0) return SP_OK;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!o.host_buffers) {
@@ -487,11 +502,11 @@ sp_status sp_check_args_ex(const sp_fused_options* options, const void* partials
   Extras x;
   x.partial_scale = o.partial_scale;
   x.addend = o.addend;
+  x.scale_layout = o.scale_layout;
   const sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps,
                              quant_mode, scale, out, out_scales, residual_out, x);
   if (st != SP_OK) return st;
-  if (o.scale_layout != SP_SCALES_ROW_MAJOR || (o.host_buffers != 0 && o.host_buffers != 1))
-    return SP_ERR_UNSUPPORTED;
+  if (o.host_buffers != 0 && o.host_buffers != 1) return SP_ERR_UNSUPPORTED;
   return SP_OK;
 }
 
@@ -525,6 +540,11 @@ int64_t sp_out_bytes(int64_t T_pad, int64_t H, int quant_mode) {
 int64_t sp_out_scales_bytes(int64_t T_pad, int64_t H, int quant_mode) {
   if (T_pad < 0 || H < 0) return -1;
   return scale_bytes_of(T_pad, H, quant_mode);
+}
+
+int64_t sp_out_scales_bytes_ex(int64_t T_pad, int64_t H, int quant_mode, int scale_layout) {
+  if (T_pad < 0 || H < 0) return -1;
+  return scale_bytes_of(T_pad, H, quant_mode, scale_layout);
 }
 
 int64_t sp_max_hidden(void) { return kMaxHidden; }

@@ -128,7 +128,7 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
   int stage = 0;
   uint32_t phase = 0;
   int parity = 0;
-  for (int64_t t = blockIdx.x; t < p.T_pad; t += gridDim.x) {
+  for (int64_t t = blockIdx.x; t < p.rows_total; t += gridDim.x) {
     if (t >= p.T_valid) {
       zero_row<kVec, kMode>(p, t, c);
       continue;
@@ -193,7 +193,7 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
   const QuantConst qc = load_quant_const<kMode>(p);
 
   int parity = 0;
-  for (int64_t t = blockIdx.x; t < p.T_pad; t += gridDim.x) {
+  for (int64_t t = blockIdx.x; t < p.rows_total; t += gridDim.x) {
     if (t >= p.T_valid) {
       zero_row<kVec, kMode>(p, t, c);
       continue;

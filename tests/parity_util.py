@@ -43,14 +43,15 @@ def _pinned(t):
     return None if t is None else t.cpu().pin_memory()
 
 
-def run_gpu_host(inp: dict, *, fill: int = 0xA5, stream=None, partial_scale: float = 1.0) -> dict:
+def run_gpu_host(inp: dict, *, fill: int = 0xA5, stream=None, partial_scale: float = 1.0,
+                 scale_layout: int = 0) -> dict:
     """Run the zero-copy entry point on pinned host copies of ``inp`` into guard-banded pinned
     host outputs pre-filled with ``fill``; returns numpy results."""
     T_pad, H, mode = inp["T_pad"], inp["H"], inp["mode"]
     hin = {k: _pinned(inp.get(k)) for k in ("partials", "residual", "weight", "bias", "addend")}
     o_bytes = sp.sp_out_bytes(T_pad, H, mode)
-    s_bytes = sp.sp_out_scales_bytes(T_pad, H, mode)
-    oshape, odt, sshape, sdt = oracle.out_layout(T_pad, H, mode)
+    s_bytes = sp.sp_out_scales_bytes_ex(T_pad, H, mode, scale_layout)
+    oshape, odt, sshape, sdt = oracle.out_layout(T_pad, H, mode, scale_layout)
     tdt = {np.uint16: torch.bfloat16, np.uint8: torch.uint8, np.float32: torch.float32}
 
     def guarded(nbytes):
@@ -68,14 +69,14 @@ def run_gpu_host(inp: dict, *, fill: int = 0xA5, stream=None, partial_scale: flo
     res_out = _view(res_m, (T_pad, H), torch.bfloat16)
     scale_t = (torch.tensor([inp["scale"]], dtype=torch.float32).pin_memory()
                if inp["scale"] is not None else None)
-    if partial_scale == 1.0 and hin["addend"] is None:
+    if partial_scale == 1.0 and hin["addend"] is None and scale_layout == 0:
         sp.sp_fused_reduce_norm_host(hin["partials"], hin["weight"], out, res_out,
                                      residual=hin["residual"], bias=hin["bias"], eps=inp["eps"],
                                      quant_mode=mode, scale=scale_t, out_scales=sc,
                                      T_valid=inp["T_valid"], stream=stream)
     else:
         opts = sp.sp_options_init(partial_scale=partial_scale, addend=hin["addend"],
-                                  host_buffers=True)
+                                  scale_layout=scale_layout, host_buffers=True)
         sp.sp_fused_reduce_norm_ex(opts, hin["partials"], hin["weight"], out, res_out,
                                    residual=hin["residual"], bias=hin["bias"], eps=inp["eps"],
                                    quant_mode=mode, scale=scale_t, out_scales=sc,
@@ -90,15 +91,15 @@ def run_gpu_host(inp: dict, *, fill: int = 0xA5, stream=None, partial_scale: flo
 
 
 def run_gpu(inp: dict, *, config: dict | None = None, fill: int = 0xA5, inplace: bool = False,
-            stream=None, partial_scale: float = 1.0) -> dict:
+            stream=None, partial_scale: float = 1.0, scale_layout: int = 0) -> dict:
     """Run the library once on inputs ``inp`` (device tensors from synth.make_inputs) into
     guard-banded outputs pre-filled with ``fill``; returns host numpy results."""
     dev = inp["partials"].device
     T_pad, H, mode = inp["T_pad"], inp["H"], inp["mode"]
     o_bytes = sp.sp_out_bytes(T_pad, H, mode)
-    s_bytes = sp.sp_out_scales_bytes(T_pad, H, mode)
+    s_bytes = sp.sp_out_scales_bytes_ex(T_pad, H, mode, scale_layout)
     out_w, out_m = guarded_empty(o_bytes, dev, fill)
-    oshape, odt, sshape, sdt = oracle.out_layout(T_pad, H, mode)
+    oshape, odt, sshape, sdt = oracle.out_layout(T_pad, H, mode, scale_layout)
     tdt = {np.uint16: torch.bfloat16, np.uint8: torch.uint8, np.float32: torch.float32}
     out = _view(out_m, oshape, tdt[odt])
     sc_w = sc = None
@@ -120,9 +121,10 @@ def run_gpu(inp: dict, *, config: dict | None = None, fill: int = 0xA5, inplace:
         scale_t = torch.tensor([inp["scale"]], dtype=torch.float32, device=dev)
     kw = dict(residual=residual, bias=inp["bias"], eps=inp["eps"], quant_mode=mode, scale=scale_t,
               out_scales=sc, T_valid=inp["T_valid"], stream=stream)
-    if partial_scale != 1.0 or inp.get("addend") is not None:
+    if partial_scale != 1.0 or inp.get("addend") is not None or scale_layout != 0:
         assert config is None
-        opts = sp.sp_options_init(partial_scale=partial_scale, addend=inp.get("addend"))
+        opts = sp.sp_options_init(partial_scale=partial_scale, addend=inp.get("addend"),
+                                  scale_layout=scale_layout)
         sp.sp_fused_reduce_norm_ex(opts, inp["partials"], inp["weight"], out, res_out, **kw)
     elif config is None:
         sp.sp_fused_reduce_norm(inp["partials"], inp["weight"], out, res_out, **kw)
@@ -144,14 +146,16 @@ def bits_of(t: torch.Tensor) -> np.ndarray:
     return t.cpu().numpy()
 
 
-def run_oracle(inp: dict, want_y: bool = True, rows=None, partial_scale: float = 1.0) -> dict:
+def run_oracle(inp: dict, want_y: bool = True, rows=None, partial_scale: float = 1.0,
+               scale_layout: int = 0) -> dict:
     to = synth.bf16_bits
     add = inp.get("addend")
     res = oracle.fused_reduce_norm(
         to(inp["partials"]), None if inp["residual"] is None else to(inp["residual"]),
         to(inp["weight"]), None if inp["bias"] is None else to(inp["bias"]), inp["eps"],
         inp["mode"], inp["scale"], inp["T_valid"], want_y=want_y, threads=CORES, rows=rows,
-        partial_scale=partial_scale, addend=None if add is None else to(add))
+        partial_scale=partial_scale, addend=None if add is None else to(add),
+        scale_layout=scale_layout)
     assert res["status"] == 0
     return res
 
@@ -207,9 +211,10 @@ def compare(gpu: dict, ref: dict, inp: dict) -> dict:
     Tv, mode = inp["T_valid"], inp["mode"]
     valid = slice(0, Tv)
     stats = {}
-    # padding rows: all zero bytes
+    swizzled = mode == "nvfp4" and gpu["out_scales"] is not None and gpu["out_scales"].ndim == 1
+    # padding rows: all zero bytes (swizzled scales: compared whole against the oracle below)
     for k in ("out", "out_scales", "residual_out"):
-        if gpu[k] is not None:
+        if gpu[k] is not None and not (k == "out_scales" and swizzled):
             pad = gpu[k][Tv:]
             assert not pad.view(np.uint8).any(), f"{k}: padding rows not zero"
     stats["residual_max_abs"] = check_bf16(gpu["residual_out"], _bf16_to_f64(ref["residual_out"]),
@@ -224,8 +229,13 @@ def compare(gpu: dict, ref: dict, inp: dict) -> dict:
             assert np.all((rel <= 1e-5) | ((g == 0) & (r == 0))), "per-token scales"
             stats["scale_max_rel"] = float(rel.max()) if rel.size else 0.0
     elif mode == "nvfp4":
-        stats["scale_code_match"] = check_codes(gpu["out_scales"][valid], ref["out_scales"][valid],
-                                                0x80, "e4m3 block scales")
+        if swizzled:  # the whole padded buffer: scales in place, padding bytes zero
+            stats["scale_code_match"] = check_codes(gpu["out_scales"], ref["out_scales"], 0x80,
+                                                    "e4m3 block scales (swizzled)")
+        else:
+            stats["scale_code_match"] = check_codes(gpu["out_scales"][valid],
+                                                    ref["out_scales"][valid], 0x80,
+                                                    "e4m3 block scales")
         stats["code_match"] = check_codes(unpack_e2m1(gpu["out"][valid]),
                                           unpack_e2m1(ref["out"][valid]), 0x8, "e2m1 out")
     return stats

@@ -66,6 +66,17 @@ def test_padding_and_shards_match_the_pr_example(lib):
         sp.sp_shard_rows(3504, 16, 16)
 
 
+def test_swizzled_scale_sizes(lib):
+    # rows padded to 128, block columns to 4
+    assert sp.sp_out_scales_bytes_ex(16384, 5120, "nvfp4", 1) == 16384 * 320
+    assert sp.sp_out_scales_bytes_ex(3500, 5120, "nvfp4", 1) == 3584 * 320
+    assert sp.sp_out_scales_bytes_ex(1, 16, "nvfp4", 1) == 128 * 4
+    assert sp.sp_out_scales_bytes_ex(200, 1008, "nvfp4", 1) == 256 * 64
+    assert sp.sp_out_scales_bytes_ex(16, 64, "nvfp4", 0) == 16 * 4
+    assert sp.sp_out_scales_bytes_ex(16, 64, "fp8_per_token", 1) == -1
+    assert sp.sp_out_scales_bytes_ex(16, 64, "nvfp4", 3) == -1
+
+
 def test_output_sizes(lib):
     assert sp.sp_out_bytes(4096, 4096, "none") == 4096 * 4096 * 2
     assert sp.sp_out_bytes(8192, 7168, "fp8_static") == 8192 * 7168
@@ -179,7 +190,14 @@ OPTION_CASES = [
     (dict(addend=A * 20 + 8), {}, "SP_ERR_ALIGNMENT"),
     (dict(addend=A * 11 + 64), {}, "SP_ERR_INVALID_ARG"),          # inside `out`
     (dict(addend=A * 13), {}, "SP_ERR_INVALID_ARG"),                # is residual_out
-    (dict(scale_layout=1), {}, "SP_ERR_UNSUPPORTED"),
+    (dict(scale_layout=1), {}, "SP_ERR_INVALID_ARG"),               # swizzle is NVFP4-only
+    (dict(scale_layout=2), {}, "SP_ERR_UNSUPPORTED"),
+    (dict(scale_layout=1), {"quant_mode": "nvfp4", "scale": A * 14}, "SP_OK"),
+    # 16 x 64 NVFP4 scales: 64 bytes row-major, 128 x 4 = 512 bytes swizzled
+    (dict(scale_layout=0), {"quant_mode": "nvfp4", "scale": A * 14,
+                            "out_scales": A * 13 - 256}, "SP_OK"),
+    (dict(scale_layout=1), {"quant_mode": "nvfp4", "scale": A * 14,
+                            "out_scales": A * 13 - 256}, "SP_ERR_INVALID_ARG"),
     (dict(host_buffers=2), {}, "SP_ERR_UNSUPPORTED"),
     (dict(addend=A * 20), {"T_pad": 18}, "SP_ERR_INVALID_ARG"),     # shape rule first
 ]

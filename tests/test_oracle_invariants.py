@@ -460,3 +460,29 @@ def test_addend_is_chunked_per_shard(mode):
                      max(0, min(S, T - 3 - r * S)), partial_scale=0.75,
                      addend=addend[r * S:(r + 1) * S].contiguous()) for r in range(tp)]
     same(full, concat(shards))
+
+
+# --------------------------------------------------------------------------- N2 swizzled scales
+@pytest.mark.parametrize("T,H", [(8, 64), (130, 80), (256, 1024), (3, 16)])
+def test_swizzled_scales_hold_exactly_the_row_major_scales(T, H):
+    """The 128x4-tile layout is a placement of the same block scales, padding zero: the swizzled
+    buffer holds every row-major scale once plus (padded size - T*H/16) zero bytes, and the
+    codes and y do not depend on the layout. (The placement map itself is checked on the GPU
+    by cuBLASLt's block-scaled GEMM reading the library's output.)"""
+    g = torch.Generator().manual_seed(T * 1000 + H)
+    tp = 2
+    T_pad = tp * -(-T // tp)
+    partials = rand_bf16(g, (tp, T_pad, H), 0.7)
+    residual = rand_bf16(g, (T_pad, H))
+    w, b = rand_bf16(g, (H,), 0.1) + 1, rand_bf16(g, (H,), 0.01)
+    args = (bits(partials), bits(residual), bits(w), bits(b), 1e-6, "nvfp4", 60.0, T)
+    flat = oracle.fused_reduce_norm(*args)
+    swz = oracle.fused_reduce_norm(*args, scale_layout=1)
+    assert flat["status"] == 0 and swz["status"] == 0
+    assert np.array_equal(flat["out"], swz["out"])
+    assert np.array_equal(flat["residual_out"], swz["residual_out"])
+    rows, cols = -(-T_pad // 128) * 128, -(-(H // 16) // 4) * 4
+    assert swz["out_scales"].shape == (rows * cols,)
+    want = np.bincount(flat["out_scales"].ravel(), minlength=256)
+    want[0] += rows * cols - T_pad * (H // 16)
+    assert np.array_equal(np.bincount(swz["out_scales"], minlength=256), want)

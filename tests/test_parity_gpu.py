@@ -186,5 +186,68 @@ def test_partial_scale_and_addend(mode, c, with_addend, with_residual, host):
     compare(a, run_oracle(inp, partial_scale=c), inp)
 
 
+@pytest.mark.parametrize("T_pad,H", [(336, 5120), (16, 80), (256, 1008), (136, 4096)])
+@pytest.mark.parametrize("host", [False, True])
+def test_swizzled_nvfp4_scales(T_pad, H, host):
+    """NVFP4 block scales in the 128x4-tile layout: padded rows and columns zero, scales in place."""
+    w = synth.workload(5)
+    inp = synth.make_inputs(w, device=DEV, T_pad=T_pad, T_valid=T_pad - 3, H=H)
+    run = run_gpu_host if host else run_gpu
+    a = run(inp, fill=0xA5, scale_layout=1)
+    b = run(inp, fill=0x5A, scale_layout=1)
+    for k in ("out", "out_scales", "residual_out"):
+        assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+    compare(a, run_oracle(inp, scale_layout=1), inp)
+
+
+E2M1_VALUES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0, -0.0, -0.5, -1.0, -1.5, -2.0, -3.0, -4.0, -6.0]
+
+
+def _dequant_nvfp4(packed: torch.Tensor, scales_rm: torch.Tensor) -> torch.Tensor:
+    lut = torch.tensor(E2M1_VALUES, dtype=torch.float64, device=packed.device)
+    codes = torch.stack([packed & 0xF, packed >> 4], dim=-1).reshape(packed.shape[0], -1).long()
+    sf = scales_rm.view(torch.float8_e4m3fn).to(torch.float64)
+    return lut[codes] * sf.repeat_interleave(16, dim=1)
+
+
+def test_swizzled_scales_feed_a_block_scaled_gemm():
+    """cuBLASLt's NVFP4 block-scaled GEMM (torch._scaled_mm) reads the library's codes and swizzled
+    scales; the product must equal the matmul of the values dequantised with the row-major
+    scales of the same call."""
+    M, K, N = 256, 1024, 256
+    w = synth.workload(5)
+    inp = synth.make_inputs(w, device=DEV, T_pad=M, T_valid=M, H=K)
+    opts = lambda layout: sp.sp_options_init(scale_layout=layout)  # noqa: E731
+    outs = {}
+    for layout in (0, 1):
+        o = sp.allocate_outputs(M, K, "nvfp4", DEV, scale_layout=layout)
+        sp.sp_fused_reduce_norm_ex(opts(layout), inp["partials"], inp["weight"], o["out"],
+                                   o["residual_out"], residual=inp["residual"], bias=inp["bias"],
+                                   quant_mode="nvfp4",
+                                   scale=torch.tensor([inp["scale"]], device=DEV),
+                                   out_scales=o["out_scales"], T_valid=M)
+        outs[layout] = o
+    torch.cuda.synchronize()
+    assert torch.equal(outs[0]["out"], outs[1]["out"])
+    g = torch.Generator(device=DEV).manual_seed(9)
+    b_codes = torch.randint(0, 256, (N, K // 2), generator=g, device=DEV, dtype=torch.uint8)
+    b_codes[(b_codes & 0xF) == 0x8] ^= 0x8  # no negative zeros
+    n_sb = 128 * -(-N // 128) * (-(-(K // 16) // 4) * 4)
+    sb = torch.full((n_sb,), 0x38, dtype=torch.uint8, device=DEV)  # every B block scale = 1.0
+    try:
+        c = torch._scaled_mm(outs[1]["out"].view(torch.float4_e2m1fn_x2),
+                             b_codes.view(torch.float4_e2m1fn_x2).t(),
+                             scale_a=outs[1]["out_scales"].view(torch.float8_e4m3fn),
+                             scale_b=sb.view(torch.float8_e4m3fn), out_dtype=torch.bfloat16)
+    except (RuntimeError, NotImplementedError) as e:
+        pytest.skip(f"no NVFP4 block-scaled GEMM in this torch build: {e}")
+    a_deq = _dequant_nvfp4(outs[0]["out"], outs[0]["out_scales"])
+    b_deq = _dequant_nvfp4(b_codes, torch.full((N, K // 16), 0x38, dtype=torch.uint8, device=DEV))
+    ref = a_deq @ b_deq.t()
+    err = (c.double() - ref).abs()
+    tol = 1e-2 * ref.abs() + 1e-2 * ref.abs().max()
+    assert bool((err <= tol).all()), f"max err {err.max().item()} vs scale {ref.abs().max().item()}"
+
+
 def test_no_device_wait_ran_out():
     assert sp.sp_device_error(clear=False) == 0
