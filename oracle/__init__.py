@@ -58,6 +58,12 @@ def load(path: str | None = None) -> ctypes.CDLL:
         fn = getattr(lib, "sp_oracle_" + name)
         fn.argtypes = [cin, cout, _i64]
         fn.restype = None
+    lib.sp_oracle_fc2_batch_ids.argtypes = [ctypes.c_int, ctypes.c_int,
+                                            ctypes.POINTER(ctypes.c_int)]
+    lib.sp_oracle_fc2_batch_ids.restype = None
+    lib.sp_oracle_fc2_reorganize.argtypes = [_u8p, ctypes.c_int, ctypes.c_int, _i64, _i64,
+                                             ctypes.c_int, _u8p]
+    lib.sp_oracle_fc2_reorganize.restype = ctypes.c_int
     _loaded[path] = lib
     return lib
 
@@ -198,3 +204,26 @@ def e2m1_encode(x, lib=None):
 
 def e2m1_decode(c, lib=None):
     return _codec("e2m1_decode", c, np.uint8, np.float64, lib)
+
+
+def fc2_batch_ids(global_tp: int, otp_size: int, lib=None) -> list[list[int]]:
+    """The reorganised batch ids: odp_size lists of otp_size token-segment indices."""
+    lib = lib or load()
+    D = global_tp // otp_size
+    ids = (ctypes.c_int * (D * otp_size))()
+    lib.sp_oracle_fc2_batch_ids(global_tp, otp_size, ids)
+    return [list(ids[j * otp_size:(j + 1) * otp_size]) for j in range(D)]
+
+
+def fc2_reorganize(x: np.ndarray, otp_size: int, lib=None) -> np.ndarray:
+    """FlashComm2 token reorganisation of x [G][N][H/G] (any dtype) into [G][N/D][H/P]."""
+    lib = lib or load()
+    G, N, F = x.shape
+    D = G // otp_size
+    x = np.ascontiguousarray(x)
+    y = np.zeros((G, N // D, F * D), x.dtype)
+    st = lib.sp_oracle_fc2_reorganize(x.view(np.uint8).ctypes.data_as(_u8p), G, otp_size, N,
+                                      F * G, x.dtype.itemsize, y.view(np.uint8).ctypes.data_as(_u8p))
+    if st != 0:
+        raise ValueError(f"oracle fc2_reorganize: status {st}")
+    return y

@@ -441,6 +441,61 @@ int sp_oracle_check_args(const uint16_t* partials, int tp, int64_t T_pad, int64_
                             quant_mode, scale, out, out_scales, residual_out));
 }
 
+// ---------------------------------------------------------------------------------------------
+// FlashComm2 token reorganisation (SP/FlashComm notes §4.2-4.4, §4.7), all ranks on one host:
+// x holds G = global_tp tensors [N][H/G] (rank r's feature slice of all N tokens, elements of
+// `esize` bytes); y receives G tensors [N/D][H/P] (P = otp_size, D = odp_size = G/P).
+// The steps as the page gives them:
+//   ids   the reorganised batch ids: D lists, list j = token segments {j, j+D, j+2D, ...}
+//         (P of the G segments of N/G tokens; [[0,2],[1,3]] for G=4, P=2);
+//   (1)   every rank cuts its local tensor into D packets, packet j = the rows of list j's
+//         segments, in list order;
+//   (2)   all_to_all inside each ODP group {gD, ..., gD+D-1}: member j receives packet j of every
+//         member m, in member order;
+//   (3)   the received [D][rows][H/G] pieces are concatenated along the feature dimension.
+// ---------------------------------------------------------------------------------------------
+extern "C" void sp_oracle_fc2_batch_ids(int global_tp, int otp_size, int* ids /* [D][P] */) {
+  const int D = global_tp / otp_size, P = otp_size;
+  for (int j = 0; j < D; ++j)
+    for (int k = 0; k < P; ++k) ids[j * P + k] = j + k * D;
+}
+
+extern "C" int sp_oracle_fc2_reorganize(const uint8_t* x, int global_tp, int otp_size, int64_t N,
+                                        int64_t H, int esize, uint8_t* y) {
+  const int G = global_tp;
+  if (G < 1 || otp_size < 1 || G % otp_size != 0 || N % G != 0 || H % G != 0 || esize < 1)
+    return kInvalidArg;
+  const int P = otp_size, D = G / P;
+  const int64_t seg = N / G, F = H / G, row_in = F * esize;
+  std::vector<int> ids(static_cast<size_t>(D) * P);
+  sp_oracle_fc2_batch_ids(G, P, ids.data());
+  // (1) packets[s][j]: [P * seg][F]
+  std::vector<std::vector<uint8_t>> packets(static_cast<size_t>(G) * D);
+  for (int s = 0; s < G; ++s) {
+    const uint8_t* local = x + static_cast<int64_t>(s) * N * row_in;
+    for (int j = 0; j < D; ++j) {
+      std::vector<uint8_t>& pk = packets[static_cast<size_t>(s) * D + j];
+      for (int k = 0; k < P; ++k) {
+        const int64_t first = ids[j * P + k] * seg;
+        pk.insert(pk.end(), local + first * row_in, local + (first + seg) * row_in);
+      }
+    }
+  }
+  // (2) all_to_all in each ODP group, then (3) concat along features
+  const int64_t rows_out = P * seg, row_out = static_cast<int64_t>(D) * row_in;
+  for (int r = 0; r < G; ++r) {
+    const int g = r / D, j = r % D;
+    uint8_t* out = y + static_cast<int64_t>(r) * rows_out * row_out;
+    for (int m = 0; m < D; ++m) {
+      const std::vector<uint8_t>& recv = packets[static_cast<size_t>(g * D + m) * D + j];
+      for (int64_t i = 0; i < rows_out; ++i)
+        std::memcpy(out + i * row_out + m * row_in, recv.data() + i * row_in,
+                    static_cast<size_t>(row_in));
+    }
+  }
+  return kOk;
+}
+
 // Codecs, element-wise over n values (for the format tests).
 void sp_oracle_bf16_encode(const double* x, uint16_t* code, int64_t n) {
   for (int64_t i = 0; i < n; ++i) code[i] = bf16_code(x[i]);

@@ -42,6 +42,8 @@ MUTANTS = {
     "no_subnormals": ("std::max(e2 - 1, emin)", "(e2 - 1)"),
     "e4m3_max_480": ("{4, 3, 7, 448.0, true}", "{4, 3, 7, 480.0, true}"),
     "bf16_saturates": ("std::ldexp(255.0, 120), false}", "std::ldexp(255.0, 120), true}"),
+    "fc2_contiguous_batch_ids": ("ids[j * P + k] = j + k * D;", "ids[j * P + k] = j * P + k;"),
+    "fc2_member_order": ("out + i * row_out + m * row_in", "out + i * row_out + (D - 1 - m) * row_in"),
     "residual_out_unrounded_sum": ("a.residual_out[t * H + j] = bf16_code(h[j]);",
                                    "a.residual_out[t * H + j] = bf16_code(h[j] - bf16_value(a.weight[j]) + 1.0);"),
 }
@@ -60,7 +62,8 @@ def _run_mutant(name: str, old: str, new: str, workdir: str) -> tuple[str, int, 
     env = dict(os.environ, SP_ORACLE_LIBRARY=lib)
     proc = subprocess.run(
         [sys.executable, "-m", "pytest", "-q", "-x", "-p", "no:cacheprovider",
-         "tests/test_oracle_codecs.py", "tests/test_oracle_invariants.py"],
+         "tests/test_oracle_codecs.py", "tests/test_oracle_invariants.py",
+         "tests/test_oracle_fc2.py"],
         cwd=ROOT, env=env, capture_output=True, text=True, timeout=600)
     return name, proc.returncode, proc.stdout[-400:]
 
