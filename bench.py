@@ -428,6 +428,7 @@ def run_ours(args) -> None:
         for name, variant in VARIANT_RUNS:
             extras[f"{name}+{variant}"] = bench_extra(lib, sp, synth, synth.workload(name),
                                                       device, stream, peak, variant)
+        extras["fc2_reorganize_G8_otp2_N8192_H7168_bf16"] = bench_fc2(lib, device, stream, peak)
 
     if rank != 0:
         return
@@ -515,6 +516,40 @@ def run_kernel_only(args) -> None:
                       "kernel_us": round(k * 1e3, 2), "GB_per_s": round(one / k / 1e6, 1),
                       "launch": sp.sp_select_launch(w["tp"], w["T_pad"], w["H"],
                                                     w["mode"]).as_dict()}), flush=True)
+
+
+def bench_fc2(lib, device, stream, peak, G=8, P=2, N=8192, H=7168) -> dict:
+    """FlashComm2 token reorganisation of [G][N][H/G] bf16 (a pure permutation: algorithmic
+    bytes = read x + write y = 2 * N * H * 2)."""
+    nbytes = N * H * 2
+    sets = max(2, -(-(4 * L2_BYTES) // (2 * nbytes)))
+    g = torch.Generator(device=device).manual_seed(7)
+    xs = [torch.randn((G, N, H // G), generator=g, device=device).to(torch.bfloat16)
+          for _ in range(sets)]
+    ys = [torch.empty((G, N // (G // P), H // P), dtype=torch.bfloat16, device=device)
+          for _ in range(sets)]
+    h = ctypes.c_void_p(stream.cuda_stream)
+    args = [(x.data_ptr(), G, P, N, H, 2, y.data_ptr(), h) for x, y in zip(xs, ys)]
+    one = 2 * nbytes
+    steps = int(min(4000, max(20, 0.05 * 6.5e12 / one)))
+    for k in range(10):
+        lib.sp_fc2_reorganize(*args[k % sets])
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for k in range(steps):
+        st = lib.sp_fc2_reorganize(*args[k % sets])
+        if st != 0:
+            raise RuntimeError(f"sp_fc2_reorganize returned {st}")
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / steps
+    gbs = one / (ms / 1e3) / 1e9
+    del xs, ys
+    torch.cuda.empty_cache()
+    return {"GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "kernel_us": round(ms * 1e3, 2), "steps": steps, "bytes": one, "sets": sets,
+            "mtokens_per_s": round(N / (ms / 1e3) / 1e6, 3)}
 
 
 # ------------------------------------------------------------------------------ reference arm

@@ -246,6 +246,29 @@ int64_t sp_out_scales_bytes(int64_t T_pad, int64_t H, int quant_mode);
 int64_t sp_out_scales_bytes_ex(int64_t T_pad, int64_t H, int quant_mode, int scale_layout);
 int64_t sp_max_hidden(void);
 
+/*
+ * FlashComm2 token reorganisation (vllm-ascend SP/FlashComm notes §4.2-4.4, worked example in
+ * §4.4), all ranks on one GPU. With G = global_tp, P = otp_size, D = odp_size = G/P,
+ * F = H/G, S = N/G:
+ *   x  [G][N][F] elements of elem_bytes bytes: rank r's feature slice of all N tokens.
+ *   y  [G][N/D][D*F]: what rank r = g*D + j holds after (1) every rank cuts its slice into D
+ *      packets by the reorganised batch ids (packet j = token segments j, j+D, j+2D, ... of S
+ *      tokens each), (2) the all_to_all inside ODP group {g*D .. g*D+D-1}, (3) the concat of the
+ *      D received pieces along the feature dimension: y[r][k*S + t][m*F + f] =
+ *      x[g*D + m][(j + k*D)*S + t][f]. The ranks {j, j+D, ...} (an OTP group) then hold the same
+ *      tokens with complementary features.
+ * Requirements: G, P >= 1, G % P == 0, N % G == 0, H % G == 0, elem_bytes in {1, 2, 4, 8}
+ * (SP_ERR_INVALID_ARG); x and y 16-byte aligned and F * elem_bytes a multiple of 16
+ * (SP_ERR_ALIGNMENT); x and y must not overlap. N == 0 launches nothing. Device pointers,
+ * asynchronous on `stream`.
+ */
+sp_status sp_fc2_reorganize(const void* x, int global_tp, int otp_size, int64_t N, int64_t H,
+                            int elem_bytes, void* y, sp_stream_t stream);
+sp_status sp_fc2_check_args(const void* x, int global_tp, int otp_size, int64_t N, int64_t H,
+                            int elem_bytes, const void* y);
+/* The reorganised batch ids: ids[j*P + k] = j + k*D (D lists of P segments; host array). */
+sp_status sp_fc2_batch_ids(int global_tp, int otp_size, int* ids /* host, [D*P] */);
+
 /* Name of a status code, e.g. "SP_ERR_ALIGNMENT"; "SP_UNKNOWN_STATUS" for other values. */
 const char* sp_status_string(int status);
 

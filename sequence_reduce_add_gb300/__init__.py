@@ -23,7 +23,8 @@ __all__ = [
     "sp_fused_reduce_norm_with_config", "sp_check_args", "sp_select_launch", "sp_pad_tokens",
     "sp_shard_rows", "sp_out_bytes", "sp_out_scales_bytes", "sp_max_hidden", "sp_status_string",
     "sp_device_error", "allocate_outputs", "LaunchConfig", "Options", "sp_options_init",
-    "sp_fused_reduce_norm_ex", "sp_check_args_ex", "sp_out_scales_bytes_ex",
+    "sp_fused_reduce_norm_ex", "sp_check_args_ex", "sp_out_scales_bytes_ex", "sp_fc2_reorganize",
+    "sp_fc2_check_args", "sp_fc2_batch_ids",
 ]
 
 QUANT_MODES = {"none": 0, "fp8_static": 1, "fp8_per_token": 2, "nvfp4": 3,
@@ -108,6 +109,14 @@ def load_library() -> ctypes.CDLL:
     lib.sp_out_scales_bytes.restype = _i64
     lib.sp_out_scales_bytes_ex.argtypes = [_i64, _i64, ctypes.c_int, ctypes.c_int]
     lib.sp_out_scales_bytes_ex.restype = _i64
+    lib.sp_fc2_reorganize.argtypes = [_vp, ctypes.c_int, ctypes.c_int, _i64, _i64, ctypes.c_int,
+                                      _vp, _vp]
+    lib.sp_fc2_reorganize.restype = ctypes.c_int
+    lib.sp_fc2_check_args.argtypes = [_vp, ctypes.c_int, ctypes.c_int, _i64, _i64, ctypes.c_int,
+                                      _vp]
+    lib.sp_fc2_check_args.restype = ctypes.c_int
+    lib.sp_fc2_batch_ids.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    lib.sp_fc2_batch_ids.restype = ctypes.c_int
     lib.sp_max_hidden.argtypes = []
     lib.sp_max_hidden.restype = _i64
     lib.sp_status_string.argtypes = [ctypes.c_int]
@@ -263,6 +272,29 @@ def sp_out_scales_bytes(T_pad: int, H: int, quant_mode) -> int:
 
 def sp_out_scales_bytes_ex(T_pad: int, H: int, quant_mode, scale_layout: int) -> int:
     return load_library().sp_out_scales_bytes_ex(T_pad, H, _mode(quant_mode), scale_layout)
+
+
+def sp_fc2_reorganize(x, otp_size: int, y, stream=None) -> None:
+    """FlashComm2 token reorganisation of x [G, N, H/G] into y [G, N/D, H/P] (CUDA tensors of
+    the same dtype; D = G / otp_size)."""
+    G, N, F = x.shape
+    st = load_library().sp_fc2_reorganize(x.data_ptr(), G, otp_size, N, F * G, x.element_size(),
+                                          y.data_ptr(), _stream_handle(stream))
+    if st != 0:
+        raise SpError(st, "sp_fc2_reorganize")
+
+
+def sp_fc2_check_args(x, global_tp, otp_size, N, H, elem_bytes, y) -> int:
+    return load_library().sp_fc2_check_args(x, global_tp, otp_size, N, H, elem_bytes, y)
+
+
+def sp_fc2_batch_ids(global_tp: int, otp_size: int) -> list[list[int]]:
+    D = global_tp // otp_size if otp_size > 0 else 0
+    ids = (ctypes.c_int * max(1, D * otp_size))()
+    st = load_library().sp_fc2_batch_ids(global_tp, otp_size, ids)
+    if st != 0:
+        raise SpError(st, "sp_fc2_batch_ids")
+    return [list(ids[j * otp_size:(j + 1) * otp_size]) for j in range(D)]
 
 
 def sp_max_hidden() -> int:

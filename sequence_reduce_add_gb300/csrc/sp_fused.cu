@@ -7,6 +7,7 @@
 #include <cstdint>
 #include <mutex>
 
+#include "sp_fc2.cuh"
 #include "sp_fused.h"
 #include "sp_kernels.cuh"
 
@@ -218,9 +219,9 @@ cudaError_t persistent_grid(Kernel kernel, int threads, int smem, int ctas_per_s
 
 // Launch with programmatic stream serialisation: the kernel may be scheduled while the previous
 // kernel of the stream finishes; it waits (griddepcontrol.wait) before touching global memory.
-template <typename Kernel>
+template <typename Kernel, typename KParams>
 cudaError_t launch_pdl(Kernel kernel, int grid, int threads, int smem, cudaStream_t stream,
-                       const spk::Params& p) {
+                       const KParams& p) {
   cudaLaunchConfig_t lc{};
   lc.gridDim = dim3(static_cast<unsigned>(grid));
   lc.blockDim = dim3(static_cast<unsigned>(threads));
@@ -540,6 +541,57 @@ int64_t sp_out_bytes(int64_t T_pad, int64_t H, int quant_mode) {
 int64_t sp_out_scales_bytes(int64_t T_pad, int64_t H, int quant_mode) {
   if (T_pad < 0 || H < 0) return -1;
   return scale_bytes_of(T_pad, H, quant_mode);
+}
+
+// ------------------------------------------------------------------ FlashComm2 reorganisation
+sp_status sp_fc2_batch_ids(int global_tp, int otp_size, int* ids) {
+  if (!ids || global_tp < 1 || otp_size < 1 || global_tp % otp_size != 0) return SP_ERR_INVALID_ARG;
+  const int D = global_tp / otp_size;
+  for (int j = 0; j < D; ++j)
+    for (int k = 0; k < otp_size; ++k) ids[j * otp_size + k] = j + k * D;
+  return SP_OK;
+}
+
+sp_status sp_fc2_check_args(const void* x, int global_tp, int otp_size, int64_t N, int64_t H,
+                            int elem_bytes, const void* y) {
+  if (global_tp < 1 || otp_size < 1 || global_tp % otp_size != 0) return SP_ERR_INVALID_ARG;
+  if (N < 0 || N % global_tp != 0 || H <= 0 || H % global_tp != 0) return SP_ERR_INVALID_ARG;
+  if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
+    return SP_ERR_INVALID_ARG;
+  if (N == 0) return SP_OK;
+  if (!x || !y) return SP_ERR_INVALID_ARG;
+  const int64_t bytes = N * H * elem_bytes;
+  if (overlaps(x, bytes, y, bytes)) return SP_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || ((H / global_tp) * elem_bytes) % 16 != 0)
+    return SP_ERR_ALIGNMENT;
+  return SP_OK;
+}
+
+sp_status sp_fc2_reorganize(const void* x, int global_tp, int otp_size, int64_t N, int64_t H,
+                            int elem_bytes, void* y, sp_stream_t stream) {
+  sp_status st = sp_fc2_check_args(x, global_tp, otp_size, N, H, elem_bytes, y);
+  if (st != SP_OK || N == 0) return st;
+  DeviceInfo* dev = nullptr;
+  st = device_info(&dev);
+  if (st != SP_OK) return st;
+  spk::Fc2Params p{};
+  p.x = static_cast<const unsigned char*>(x);
+  p.y = static_cast<unsigned char*>(y);
+  p.N = N;
+  p.pieces = static_cast<int64_t>(global_tp) * N;
+  p.S = N / global_tp;
+  p.P = otp_size;
+  p.D = global_tp / otp_size;
+  p.piece_vecs = static_cast<int>((H / global_tp) * elem_bytes / 16);
+  int grid = 0;
+  cudaError_t e = persistent_grid(spk::k_fc2_reorganize, spk::kFc2Threads, 0, 8,
+                                  (p.pieces + spk::kFc2Threads / 32 - 1) / (spk::kFc2Threads / 32),
+                                  dev, &grid);
+  if (e == cudaSuccess)
+    e = launch_pdl(spk::k_fc2_reorganize, grid, spk::kFc2Threads, 0,
+                   reinterpret_cast<cudaStream_t>(stream), p);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
 }
 
 int64_t sp_out_scales_bytes_ex(int64_t T_pad, int64_t H, int quant_mode, int scale_layout) {

@@ -215,3 +215,37 @@ def test_option_checks(lib, opt, kw, want):
                              a["residual"], a["weight"], a["bias"], a["eps"], a["quant_mode"],
                              a["scale"], a["out"], a["out_scales"], a["residual_out"])
     assert sp.sp_status_string(st) == want
+
+
+def test_fc2_batch_ids_match_the_page(lib):
+    with open(os.path.join(ROOT, "tests", "golden", "fc2_reorganize_tp4_otp2.json")) as f:
+        gold = json.load(f)
+    assert sp.sp_fc2_batch_ids(gold["global_tp"], gold["otp_size"]) == gold["batch_ids"]
+    assert sp.sp_fc2_batch_ids(8, 2) == [[0, 4], [1, 5], [2, 6], [3, 7]]
+    assert sp.sp_fc2_batch_ids(8, 8) == [[0, 1, 2, 3, 4, 5, 6, 7]]
+    with pytest.raises(sp.SpError):
+        sp.sp_fc2_batch_ids(6, 4)
+
+
+FC2_CASES = [
+    (dict(), "SP_OK"),
+    (dict(global_tp=0), "SP_ERR_INVALID_ARG"),
+    (dict(otp_size=3), "SP_ERR_INVALID_ARG"),          # 8 % 3
+    (dict(N=100), "SP_ERR_INVALID_ARG"),               # 100 % 8
+    (dict(H=1020), "SP_ERR_INVALID_ARG"),              # 1020 % 8
+    (dict(elem_bytes=3), "SP_ERR_INVALID_ARG"),
+    (dict(x=None), "SP_ERR_INVALID_ARG"),
+    (dict(y=A + 4096), "SP_ERR_INVALID_ARG"),          # overlaps x
+    (dict(y=A * 64 + 8), "SP_ERR_ALIGNMENT"),
+    (dict(H=8 * 4), "SP_ERR_ALIGNMENT"),               # 4 bf16 per slice = 8 bytes
+    (dict(N=0, x=None, y=None), "SP_OK"),
+]
+
+
+@pytest.mark.parametrize("kw,want", FC2_CASES)
+def test_fc2_argument_checks(lib, kw, want):
+    a = dict(x=A, global_tp=8, otp_size=2, N=128, H=1024, elem_bytes=2, y=A * 64)
+    a.update(kw)
+    st = sp.sp_fc2_check_args(a["x"], a["global_tp"], a["otp_size"], a["N"], a["H"],
+                              a["elem_bytes"], a["y"])
+    assert sp.sp_status_string(st) == want
