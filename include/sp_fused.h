@@ -283,6 +283,15 @@ const char* sp_status_string(int status);
 enum { SP_DEVICE_ERR_WAIT_TIMEOUT = 1 };
 sp_status sp_device_error(uint32_t* flags /* host, out */, int clear);
 
+/*
+ * sp_selftest_wait_timeout — exercises that timeout path on the current device: one warp waits,
+ * with a limit of `limit_ns` (1 ns .. 2 s), on a shared-memory barrier that nothing completes;
+ * the wait gives up, sets SP_DEVICE_ERR_WAIT_TIMEOUT in the device error word and the kernel
+ * ends normally (the context stays usable). Asynchronous on `stream`; SP_ERR_INVALID_ARG for a
+ * limit out of range.
+ */
+sp_status sp_selftest_wait_timeout(uint64_t limit_ns, sp_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

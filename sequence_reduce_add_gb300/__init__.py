@@ -24,7 +24,7 @@ __all__ = [
     "sp_shard_rows", "sp_out_bytes", "sp_out_scales_bytes", "sp_max_hidden", "sp_status_string",
     "sp_device_error", "allocate_outputs", "LaunchConfig", "Options", "sp_options_init",
     "sp_fused_reduce_norm_ex", "sp_check_args_ex", "sp_out_scales_bytes_ex", "sp_fc2_reorganize",
-    "sp_fc2_check_args", "sp_fc2_batch_ids",
+    "sp_fc2_check_args", "sp_fc2_batch_ids", "sp_selftest_wait_timeout",
 ]
 
 QUANT_MODES = {"none": 0, "fp8_static": 1, "fp8_per_token": 2, "nvfp4": 3,
@@ -123,6 +123,8 @@ def load_library() -> ctypes.CDLL:
     lib.sp_status_string.restype = ctypes.c_char_p
     lib.sp_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]
     lib.sp_device_error.restype = ctypes.c_int
+    lib.sp_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _vp]
+    lib.sp_selftest_wait_timeout.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -311,6 +313,13 @@ def sp_device_error(clear: bool = True) -> int:
     if st != 0:
         raise SpError(st, "sp_device_error")
     return flags.value
+
+
+def sp_selftest_wait_timeout(limit_ns: int, stream=None) -> None:
+    """Run the bounded-wait timeout self-test (see include/sp_fused.h)."""
+    st = load_library().sp_selftest_wait_timeout(limit_ns, _stream_handle(stream))
+    if st != 0:
+        raise SpError(st, "sp_selftest_wait_timeout")
 
 
 def allocate_outputs(T_pad: int, H: int, quant_mode, device, residual_out: bool = True,

@@ -226,16 +226,17 @@ __device__ __forceinline__ uint64_t global_timer_ns() {
 }
 
 // Wait for the phase of parity `parity` of barrier `bar` to complete. Gives up (returns false)
-// after kWaitLimitNs, or as soon as *abort is set when `abort` is given.
+// after `limit_ns`, or as soon as *abort is set when `abort` is given.
 __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  const volatile int* abort) {
+                                                  const volatile int* abort,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   if (mbar_try_wait_sleep(bar, parity, kWaitSleepHintNs)) return true;
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     if (mbar_try_wait_sleep(bar, parity, kWaitSleepHintNs)) return true;
     if (abort && *abort) return false;
-    if (global_timer_ns() - t0 > kWaitLimitNs) return false;
+    if (global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

@@ -612,6 +612,12 @@ const char* sp_status_string(int status) {
   }
 }
 
+sp_status sp_selftest_wait_timeout(uint64_t limit_ns, sp_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > spk::kWaitLimitNs) return SP_ERR_INVALID_ARG;
+  spk::k_selftest_wait_timeout<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(limit_ns);
+  return cudaGetLastError() == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+}
+
 sp_status sp_device_error(uint32_t* flags, int clear) {
   if (!flags) return SP_ERR_INVALID_ARG;
   unsigned int v = 0;

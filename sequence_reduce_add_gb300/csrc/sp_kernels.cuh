@@ -254,4 +254,19 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
   }
 }
 
+// ----------------------------------------------------------------------------------- self-test
+// The timeout path of the bounded waits, on the GPU: one warp waits, with the given limit, on an
+// mbarrier that nothing arrives at. The wait must give up, record SP_DEVICE_ERR_WAIT_TIMEOUT in
+// the device error word and let the kernel finish normally.
+__global__ void k_selftest_wait_timeout(uint64_t limit_ns) {
+  __shared__ uint64_t bar;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_addr(&bar), 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  const bool done = mbar_wait_bounded(smem_addr(&bar), 0, nullptr, limit_ns);
+  if (!done && threadIdx.x == 0) atomicOr(&g_error_flags, kErrWaitTimeout);
+}
+
 }  // namespace spk
