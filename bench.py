@@ -306,7 +306,7 @@ class OracleRunner:
         t0 = time.perf_counter()
         r = self.oracle.fused_reduce_norm(self.parts, self.res, self.wt, self.bs, 1e-6,
                                           self.w["mode"], self.scale, Tv, rows=rows,
-                                          threads=self.cores, buffers=self.buffers)
+                                          threads=min(self.cores, nrows), buffers=self.buffers)
         dt = time.perf_counter() - t0
         assert r["status"] == 0
         self.buffers = r
@@ -314,7 +314,9 @@ class OracleRunner:
         return dt, algorithmic_bytes(tp, nrows, nrows, H, self.w["mode"], self.res is not None)
 
     def rows_for(self, seconds: float) -> int:
-        probe = min(self.w["T_valid"], max(self.cores, 32))
+        """Rows that take about `seconds`, from a probe of 8 rows per thread."""
+        probe = min(self.w["T_valid"], 8 * self.cores)
+        self.run(probe)  # warm caches and the library
         dt, _ = self.run(probe)
         return max(1, int(probe * seconds / max(dt, 1e-6)))
 
@@ -491,16 +493,30 @@ def bench_extra(lib, sp, synth, w, device, stream, peak, variant: str | None = N
     return res
 
 
+FC2_WORKLOAD = "fc2_reorganize_G8_otp2_N8192_H7168_bf16"
+
+
 def run_kernel_only(args) -> None:
     """Warm-up and timed launches of the workload's kernel only, rotating over resident sets;
-    prints a short JSON line (the launch sequence that profiler captures are taken from)."""
+    prints a short JSON line (the launch sequence that profiler captures are taken from).
+    --rows R keeps the workload's shape and mode but only its first R padded rows (a smaller
+    capture of the same kernel)."""
     import sequence_reduce_add_gb300 as sp
     from sequence_reduce_add_gb300 import build as sp_build
     from sequence_reduce_add_gb300 import synth
     sp_build.build()
     lib = sp.load_library()
     device = torch.device("cuda", 0)
+    if args.workload == FC2_WORKLOAD:
+        stream = torch.cuda.Stream(device=device)
+        r = bench_fc2(lib, device, stream, measured_peak()[0])
+        print(json.dumps({"workload": FC2_WORKLOAD, **r}), flush=True)
+        return
     w = synth.workload(args.workload if not str(args.workload).isdigit() else int(args.workload))
+    if args.rows:  # a multiple of tp, with as many padding rows as the full workload
+        pad = w["T_pad"] - w["T_valid"]
+        w["T_pad"] = max(w["tp"], min(w["T_pad"], args.rows) // w["tp"] * w["tp"])
+        w["T_valid"] = max(0, w["T_pad"] - pad)
     base = Problem(w, synth.BASE_SEED + 1 + synth.WORKLOADS.index(
         next(x for x in synth.WORKLOADS if x["name"] == w["name"])), device, sp)
     sets = max(2, min(8, -(-(4 * L2_BYTES) // base.nbytes())))
@@ -611,6 +627,8 @@ def main() -> None:
     ap.add_argument("--no-extras", action="store_true")
     ap.add_argument("--kernel-only", action="store_true",
                     help="only warm-up + timed kernel launches of the workload (for profilers)")
+    ap.add_argument("--rows", type=int, default=0,
+                    help="with --kernel-only: use only the first ROWS padded rows")
     ap.add_argument("--reference-budget-s", type=float, default=60.0,
                     help="CPU seconds for the whole reference-arm run (bounded row samples)")
     args = ap.parse_args()
