@@ -87,17 +87,56 @@ __device__ __forceinline__ void stg_stream(void* p, uint32_t v) {
   asm volatile("st.global.cs.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
 
+// ---------------------------------------------------------------- paired fp32 arithmetic
+// Blackwell's packed fp32x2 instructions: each lane is an ordinary IEEE binary32 operation with
+// round-to-nearest-even, so (a0, a1) op (b0, b1) equals the two scalar operations bit for bit,
+// at half the instruction count.
+__device__ __forceinline__ void add2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b;\n\t"
+      "mov.b64 a, {%0, %1};\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "add.rn.f32x2 a, a, b;\n\t"
+      "mov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
+__device__ __forceinline__ void mul2(float& a0, float& a1, float b0, float b1) {
+  asm("{\n\t.reg .b64 a, b;\n\t"
+      "mov.b64 a, {%0, %1};\n\t"
+      "mov.b64 b, {%2, %3};\n\t"
+      "mul.rn.f32x2 a, a, b;\n\t"
+      "mov.b64 {%0, %1}, a;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "f"(b0), "f"(b1));
+}
+
+// (c0, c1) += (a0, a1) * (b0, b1), each lane one fused multiply-add
+__device__ __forceinline__ void fma2(float& c0, float& c1, float a0, float a1, float b0,
+                                     float b1) {
+  asm("{\n\t.reg .b64 a, b, c;\n\t"
+      "mov.b64 a, {%2, %3};\n\t"
+      "mov.b64 b, {%4, %5};\n\t"
+      "mov.b64 c, {%0, %1};\n\t"
+      "fma.rn.f32x2 c, a, b, c;\n\t"
+      "mov.b64 {%0, %1}, c;\n\t}"
+      : "+f"(c0), "+f"(c1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
+// Eight values times one factor.
+__device__ __forceinline__ void scale8(float (&v)[8], float f) {
+#pragma unroll
+  for (int e = 0; e < 8; e += 2) mul2(v[e], v[e + 1], f, f);
+}
+
 // ---------------------------------------------------------------- conversions
 // bf16 -> fp32 is exact: the bf16 pattern is the top half of the binary32 pattern.
 __device__ __forceinline__ void add_bf16x8(const uint4 v, float (&acc)[8]) {
-  acc[0] += __uint_as_float(v.x << 16);
-  acc[1] += __uint_as_float(v.x & 0xFFFF0000u);
-  acc[2] += __uint_as_float(v.y << 16);
-  acc[3] += __uint_as_float(v.y & 0xFFFF0000u);
-  acc[4] += __uint_as_float(v.z << 16);
-  acc[5] += __uint_as_float(v.z & 0xFFFF0000u);
-  acc[6] += __uint_as_float(v.w << 16);
-  acc[7] += __uint_as_float(v.w & 0xFFFF0000u);
+  add2(acc[0], acc[1], __uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u));
+  add2(acc[2], acc[3], __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+  add2(acc[4], acc[5], __uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u));
+  add2(acc[6], acc[7], __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 v, float (&f)[8]) {
@@ -384,14 +423,15 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
                                           const uint4 (&w)[kVec], const QuantConst& qc,
                                           RedSlot* slots, int parity, int c, int abort) {
   const int64_t H = p.H;
-  float ss = 0.0f;
+  float ss0 = 0.0f, ss1 = 0.0f;  // sums of squares of the even and the odd elements
 #pragma unroll
   for (int k = 0; k < kVec; ++k) {
     const int v = c + k * p.nthreads;
     if (v < p.nvec) stg_stream(p.residual_out + t * H + v * 8, pack_bf16x8(h[k]));
 #pragma unroll
-    for (int e = 0; e < 8; ++e) ss += h[k][e] * h[k][e];
+    for (int e = 0; e < 8; e += 2) fma2(ss0, ss1, h[k][e], h[k][e + 1], h[k][e], h[k][e + 1]);
   }
+  const float ss = ss0 + ss1;
   // h <- h * w (the weight is applied before the common factor 1/rms)
   float mx = 0.0f;
 #pragma unroll
@@ -413,18 +453,16 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
       const int v = c + k * p.nthreads;
-      float y[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) y[e] = h[k][e] * rinv;
-      if (v < p.nvec) stg_stream(static_cast<uint16_t*>(p.out) + t * H + v * 8, pack_bf16x8(y));
+      scale8(h[k], rinv);
+      if (v < p.nvec) stg_stream(static_cast<uint16_t*>(p.out) + t * H + v * 8, pack_bf16x8(h[k]));
     }
   } else if (kMode == kModeFp8Static) {
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
       const int v = c + k * p.nthreads;
-      float q[8];
-#pragma unroll
-      for (int e = 0; e < 8; ++e) q[e] = (h[k][e] * rinv) * qc.inv_scale;
+      float* q = h[k];
+      scale8(h[k], rinv);
+      scale8(h[k], qc.inv_scale);
       if (v < p.nvec)
         stg_stream(static_cast<uint8_t*>(p.out) + t * H + v * 8,
                    make_uint2(pack_e4m3x4(q[0], q[1], q[2], q[3]),

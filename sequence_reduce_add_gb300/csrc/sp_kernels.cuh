@@ -160,9 +160,7 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
       }
       if (seg + 1 == p.tp && p.partial_scale != 1.0f) {  // the reduced partial sum is complete
 #pragma unroll
-        for (int k = 0; k < kVec; ++k)
-#pragma unroll
-          for (int e = 0; e < 8; ++e) h[k][e] *= p.partial_scale;
+        for (int k = 0; k < kVec; ++k) scale8(h[k], p.partial_scale);
       }
     }
     uint4 w[kVec];
@@ -229,9 +227,7 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
     }
     if (p.partial_scale != 1.0f) {
 #pragma unroll
-      for (int k = 0; k < kVec; ++k)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) h[k][e] *= p.partial_scale;
+      for (int k = 0; k < kVec; ++k) scale8(h[k], p.partial_scale);
     }
     if (p.residual) {
 #pragma unroll
