@@ -49,7 +49,7 @@ struct Params {
 };
 
 // Per-warp slot of the row reduction: sum of squares, max |h*w| and an abort vote.
-struct RedSlot {
+struct __align__(16) RedSlot {
   float ss;
   float mx;
   int abort;
@@ -342,9 +342,10 @@ __device__ __forceinline__ float2 row_reduce(float ss, float mx, int abort, RedS
   float tss = 0.0f, tmx = 0.0f;
   int ab = 0;
   for (int w = 0; w < (nthreads >> 5); ++w) {
-    tss += s[w].ss;
-    if (kWithMax) tmx = fmaxf(tmx, s[w].mx);
-    ab |= s[w].abort;
+    const float4 slot = *reinterpret_cast<const float4*>(&s[w]);  // one 16-byte load
+    tss += slot.x;
+    if (kWithMax) tmx = fmaxf(tmx, slot.y);
+    ab |= __float_as_int(slot.z);
   }
   *abort_all = ab;
   return make_float2(tss, tmx);
@@ -457,12 +458,12 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
       if (v < p.nvec) stg_stream(static_cast<uint16_t*>(p.out) + t * H + v * 8, pack_bf16x8(h[k]));
     }
   } else if (kMode == kModeFp8Static) {
+    const float rinv_q = rinv * qc.inv_scale;  // y / scale = h*w * (rinv / scale)
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
       const int v = c + k * p.nthreads;
       float* q = h[k];
-      scale8(h[k], rinv);
-      scale8(h[k], qc.inv_scale);
+      scale8(h[k], rinv_q);
       if (v < p.nvec)
         stg_stream(static_cast<uint8_t*>(p.out) + t * H + v * 8,
                    make_uint2(pack_e4m3x4(q[0], q[1], q[2], q[3]),
