@@ -251,3 +251,67 @@ def test_swizzled_scales_feed_a_block_scaled_gemm():
 
 def test_no_device_wait_ran_out():
     assert sp.sp_device_error(clear=False) == 0
+
+
+def _call(inp, outs, stream=None):
+    sc = None if inp["scale"] is None else torch.tensor([inp["scale"]], device=DEV)
+    sp.sp_fused_reduce_norm(inp["partials"], inp["weight"], outs["out"], outs["residual_out"],
+                            residual=inp["residual"], bias=inp["bias"], eps=inp["eps"],
+                            quant_mode=inp["mode"], scale=sc, out_scales=outs["out_scales"],
+                            T_valid=inp["T_valid"], stream=stream)
+
+
+def _host(outs):
+    from parity_util import bits_of
+    return {k: (None if v is None else bits_of(v)) for k, v in outs.items()}
+
+
+@pytest.mark.parametrize("wi", [2, 4, 5])
+def test_cuda_graph_capture_and_replay(wi):
+    """The call captured in a CUDA graph (with its programmatic-dependent-launch attribute) and
+    replayed after the input buffers were refilled computes on the new contents."""
+    w = synth.workload(wi)
+    inp = _small(w)
+    outs = sp.allocate_outputs(inp["T_pad"], inp["H"], inp["mode"], DEV)
+    scale = None if inp["scale"] is None else torch.tensor([inp["scale"]], device=DEV)
+    s = torch.cuda.Stream(device=DEV)
+    g = torch.cuda.CUDAGraph()
+
+    def call():
+        sp.sp_fused_reduce_norm(inp["partials"], inp["weight"], outs["out"], outs["residual_out"],
+                                residual=inp["residual"], bias=inp["bias"], eps=inp["eps"],
+                                quant_mode=inp["mode"], scale=scale,
+                                out_scales=outs["out_scales"], T_valid=inp["T_valid"])
+
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        call()
+        call()  # two launches: a programmatic edge inside the graph
+    fresh = synth.make_inputs(w, device=DEV, T_pad=inp["T_pad"], T_valid=inp["T_valid"],
+                              seed=inp["seed"] + 77)
+    for k in ("partials", "residual", "weight", "bias"):
+        inp[k].copy_(fresh[k])
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    compare(_host(outs), run_oracle(fresh), fresh)
+
+
+def test_two_streams_concurrently():
+    """Calls on two streams at once, on different buffers, each give their own correct result."""
+    w = synth.workload(3)
+    a = _small(w)
+    b = synth.make_inputs(w, device=DEV, T_pad=a["T_pad"], T_valid=a["T_valid"] - 4,
+                          seed=a["seed"] + 5)
+    oa = sp.allocate_outputs(a["T_pad"], a["H"], a["mode"], DEV)
+    ob = sp.allocate_outputs(b["T_pad"], b["H"], b["mode"], DEV)
+    sa, sb = torch.cuda.Stream(device=DEV), torch.cuda.Stream(device=DEV)
+    torch.cuda.synchronize()
+    for _ in range(20):
+        _call(a, oa, stream=sa)
+        _call(b, ob, stream=sb)
+    torch.cuda.synchronize()
+    compare(_host(oa), run_oracle(a), a)
+    compare(_host(ob), run_oracle(b), b)
