@@ -483,10 +483,32 @@ def bench_extra(lib, sp, synth, w, device, stream, peak, variant: str | None = N
     _, launches = time_kernel_loop(lib, problems, min(steps, 100), stream, True)
     k = total / steps
     gbs = one / (k / 1e3) / 1e9
+    graph_us = None
+    if one < 64e6:  # small enough to be launch-bound: also time launches replayed from a graph
+        g = torch.cuda.CUDAGraph()
+        fn = getattr(lib, problems[0].fn_name)
+        with torch.cuda.stream(stream):
+            with torch.cuda.graph(g, stream=stream):
+                hh = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+                for i in range(100):
+                    fn(*problems[i % len(problems)].args, hh)
+        torch.cuda.synchronize()
+        for _ in range(3):
+            g.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        with torch.cuda.stream(stream):
+            for _ in range(20):
+                g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        graph_us = round(a.elapsed_time(b) / 2000 * 1e3, 2)
+        del g
     res = {"GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
            "mtokens_per_s": round(w["T_valid"] / (k / 1e3) / 1e6, 3), "kernel_us": round(k * 1e3, 2),
            "isolated_launch_us": round(float(np.mean(launches)) * 1e3, 2), "steps": steps,
-           "bytes": one,
+           "bytes": one, "cuda_graph_us_per_launch": graph_us,
            "sets": len(problems)}
     del problems
     torch.cuda.empty_cache()
