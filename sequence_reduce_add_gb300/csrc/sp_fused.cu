@@ -107,11 +107,17 @@ sp_status check(const void* partials, int tp, int64_t T_pad, int64_t T_valid, in
 constexpr int kMaxDevices = 64;
 constexpr int kSmemPerSm = 233472;   // 228 KiB of shared memory per SM
 constexpr int kSmemPerCtaMax = 232448;  // 227 KiB opt-in limit per CTA
+// FlashComm2 reorganisation: bulk-copy tiles of at most this many bytes, ring stages per CTA,
+// CTAs per SM. Pieces larger than a tile go through the register kernel.
+constexpr int kFc2TileBytes = 24576;
+constexpr int kFc2Stages = 3;
+constexpr int kFc2CtasPerSm = 3;
 constexpr int kSmemReservedPerCta = 1024;
 
 struct DeviceInfo {
   int sms = 0;
   std::atomic<bool> staged_attr_set[3][4] = {};
+  std::atomic<bool> fc2_attr_set{false};
 };
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_devices_mutex;
@@ -594,13 +600,39 @@ sp_status sp_fc2_reorganize(const void* x, int global_tp, int otp_size, int64_t 
   p.P = otp_size;
   p.D = global_tp / otp_size;
   p.piece_vecs = static_cast<int>((H / global_tp) * elem_bytes / 16);
+  p.piece_bytes = static_cast<uint32_t>(p.piece_vecs) * 16u;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   int grid = 0;
-  cudaError_t e = persistent_grid(spk::k_fc2_reorganize, spk::kFc2Threads, 0, 8,
-                                  (p.pieces + spk::kFc2Threads / 32 - 1) / (spk::kFc2Threads / 32),
-                                  dev, &grid);
-  if (e == cudaSuccess)
-    e = launch_pdl(spk::k_fc2_reorganize, grid, spk::kFc2Threads, 0,
-                   reinterpret_cast<cudaStream_t>(stream), p);
+  cudaError_t e = cudaSuccess;
+  if (p.piece_bytes <= static_cast<uint32_t>(kFc2TileBytes)) {
+    // Bulk-copy ring of kFc2Stages tiles of whole pieces, at most kFc2TileBytes each.
+    const int max_q = kFc2TileBytes / static_cast<int>(p.piece_bytes);
+    p.stages = kFc2Stages;
+    p.stage_bytes = (static_cast<uint32_t>(max_q) * p.piece_bytes + 127u) & ~127u;
+    const int smem = spk::kFc2RingOffset + p.stages * static_cast<int>(p.stage_bytes);
+    if (!dev->fc2_attr_set.load(std::memory_order_acquire)) {
+      e = cudaFuncSetAttribute(spk::k_fc2_bulk, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemPerCtaMax);
+      if (e == cudaSuccess) dev->fc2_attr_set.store(true, std::memory_order_release);
+    }
+    if (e == cudaSuccess)
+      e = persistent_grid(spk::k_fc2_bulk, 32, smem, kFc2CtasPerSm,
+                          (p.pieces + max_q - 1) / max_q, dev, &grid);
+    if (e == cudaSuccess) {
+      // Every CTA gets the same number of tiles: the fewest rounds of at most max_q pieces
+      // that cover all pieces, with the pieces spread evenly over those tiles.
+      const int64_t rounds = (p.pieces + static_cast<int64_t>(grid) * max_q - 1) /
+                             (static_cast<int64_t>(grid) * max_q);
+      p.tile_pieces = static_cast<int>((p.pieces + rounds * grid - 1) / (rounds * grid));
+      p.tiles = (p.pieces + p.tile_pieces - 1) / p.tile_pieces;
+      e = launch_pdl(spk::k_fc2_bulk, grid, 32, smem, s, p);
+    }
+  } else {
+    e = persistent_grid(spk::k_fc2_reorganize, spk::kFc2Threads, 0, 8,
+                        (p.pieces + spk::kFc2Threads / 32 - 1) / (spk::kFc2Threads / 32), dev,
+                        &grid);
+    if (e == cudaSuccess) e = launch_pdl(spk::k_fc2_reorganize, grid, spk::kFc2Threads, 0, s, p);
+  }
   if (e == cudaSuccess) e = cudaGetLastError();
   return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
 }

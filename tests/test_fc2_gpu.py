@@ -23,6 +23,9 @@ GUARD = 4096
     (8, 2, 8 * 40, 8 * 64, torch.uint8),           # 1-byte elements (e.g. FP8 activations)
     (8, 2, 8 * 40, 8 * 32, torch.float32),
     (8, 2, 8 * 512, 8 * 896, torch.bfloat16),      # 4096 tokens, H = 7168
+    (8, 2, 8 * 1400, 8 * 256, torch.bfloat16),     # several ring passes per CTA
+    (4, 2, 4 * 3, 4 * 8, torch.bfloat16),          # 16-byte pieces, one ragged tile
+    (2, 1, 2 * 5, 2 * 8704, torch.bfloat16),       # pieces larger than a ring stage
 ])
 def test_fc2_reorganize_matches_oracle(G, P, N, H, dtype):
     D = G // P
