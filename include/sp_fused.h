@@ -106,8 +106,8 @@ typedef enum sp_quant_mode {
  * Every non-NULL pointer must be 16-byte aligned (SP_ERR_ALIGNMENT). No output may overlap an
  * input or another output (SP_ERR_INVALID_ARG), except residual_out == residual.
  * Checks run in this order and the first failure is returned: quant_mode, shapes (tp, T_pad,
- * T_valid, H), eps, required pointers, overlaps, alignment, H <= sp_max_hidden(). T_pad == 0
- * is a valid call that launches nothing.
+ * T_valid, H, and tp * T_pad * H * 2 <= 2^62 bytes), eps, required pointers, overlaps,
+ * alignment, H <= sp_max_hidden(). T_pad == 0 is a valid call that launches nothing.
  * Returns SP_OK once the kernel is enqueued, or the failed check's status, or SP_ERR_CUDA.
  */
 sp_status sp_fused_reduce_norm(const void* partials, int tp, int64_t T_pad, int64_t T_valid,
@@ -257,8 +257,8 @@ int64_t sp_max_hidden(void);
  *      D received pieces along the feature dimension: y[r][k*S + t][m*F + f] =
  *      x[g*D + m][(j + k*D)*S + t][f]. The ranks {j, j+D, ...} (an OTP group) then hold the same
  *      tokens with complementary features.
- * Requirements: G, P >= 1, G % P == 0, N % G == 0, H % G == 0, elem_bytes in {1, 2, 4, 8}
- * (SP_ERR_INVALID_ARG); x and y 16-byte aligned and F * elem_bytes a multiple of 16
+ * Requirements: G, P >= 1, G % P == 0, N % G == 0, H % G == 0, elem_bytes in {1, 2, 4, 8},
+ * N * H * elem_bytes <= 2^62 (SP_ERR_INVALID_ARG); x and y 16-byte aligned and F * elem_bytes a multiple of 16
  * (SP_ERR_ALIGNMENT); x and y must not overlap. N == 0 launches nothing. Device pointers,
  * asynchronous on `stream`.
  */
@@ -273,10 +273,11 @@ sp_status sp_fc2_batch_ids(int global_tp, int otp_size, int* ids /* host, [D*P] 
 const char* sp_status_string(int status);
 
 /*
- * Device-side error word. The staged kernel's waits on its shared-memory ring are bounded in
- * time; a wait that runs out (which only a hardware or runtime fault could cause) sets
- * SP_DEVICE_ERR_WAIT_TIMEOUT here, abandons the launch after letting its copies in flight
- * land, and the row it was on holds undefined values. sp_device_error reads (and, when
+ * Device-side error word. The waits of the staged kernel and of the reorganisation kernel on
+ * their shared-memory rings are bounded in time; a wait that runs out (which only a hardware or
+ * runtime fault could cause) sets SP_DEVICE_ERR_WAIT_TIMEOUT here, abandons the launch after
+ * letting its copies in flight land, and the rows (or output tiles) it had not finished hold
+ * undefined values. sp_device_error reads (and, when
  * `clear` is non-zero, resets) the word of the current device; it synchronises with the
  * device. SP_ERR_CUDA if the runtime call fails.
  */

@@ -215,6 +215,9 @@ int validate(const Args& a) {
   if (a.T_pad % a.tp != 0) return kInvalidArg;
   if (a.H <= 0 || a.H % 8 != 0) return kInvalidArg;
   if (a.mode == kNvfp4 && a.H % 16 != 0) return kInvalidArg;
+  // The partials (the largest buffer, tp * T_pad * H bf16) stay below 2^62 bytes, so that every
+  // byte count below fits in int64.
+  if (a.T_pad > (int64_t{1} << 62) / (2 * a.H) / a.tp) return kInvalidArg;
   if (!(a.eps > 0.0f) || !std::isfinite(a.eps)) return kInvalidArg;
   if (a.T_pad == 0) return kOk;
   if (!a.partials || !a.weight || !a.out || !a.residual_out) return kInvalidArg;

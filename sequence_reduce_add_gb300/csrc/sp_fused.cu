@@ -14,6 +14,9 @@
 namespace {
 
 constexpr int64_t kMaxHidden = 8 * 4 * spk::kMaxConsumerThreads;  // VEC 4 x 512 threads: 16384
+// Largest byte size of any one buffer (tp * T_pad * H * 2 for the partials): keeps every size
+// and address computation of the checks and kernels inside int64.
+constexpr int64_t kMaxBufferBytes = int64_t{1} << 62;
 
 // ------------------------------------------------------------------------------ checks
 int64_t out_bytes_of(int64_t T_pad, int64_t H, int mode) {
@@ -71,6 +74,7 @@ sp_status check(const void* partials, int tp, int64_t T_pad, int64_t T_valid, in
   if (T_pad % tp != 0) return SP_ERR_INVALID_ARG;
   if (H <= 0 || H % 8 != 0) return SP_ERR_INVALID_ARG;
   if (mode == SP_QUANT_NVFP4 && H % 16 != 0) return SP_ERR_INVALID_ARG;
+  if (T_pad > kMaxBufferBytes / (2 * H) / tp) return SP_ERR_INVALID_ARG;  // partials' bytes
   if (!(eps > 0.0f) || !std::isfinite(eps)) return SP_ERR_INVALID_ARG;
   if (!std::isfinite(x.partial_scale)) return SP_ERR_INVALID_ARG;
   if (x.scale_layout != SP_SCALES_ROW_MAJOR && x.scale_layout != SP_SCALES_SWIZZLED_128X4)
@@ -367,7 +371,8 @@ extern "C" {
 sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
                            sp_launch_config* config) {
   (void)tp;
-  if (!config || H <= 0 || H % 8 != 0 || T_pad < 0) return SP_ERR_INVALID_ARG;
+  if (!config || H <= 0 || H % 8 != 0 || T_pad < 0 || T_pad > kMaxBufferBytes / (2 * H))
+    return SP_ERR_INVALID_ARG;
   if (quant_mode < SP_QUANT_NONE || quant_mode > SP_QUANT_FP8_DYNAMIC_PER_TENSOR)
     return SP_ERR_INVALID_ARG;
   if (H > kMaxHidden) return SP_ERR_UNSUPPORTED;
@@ -575,6 +580,7 @@ sp_status sp_fc2_check_args(const void* x, int global_tp, int otp_size, int64_t 
   if (N < 0 || N % global_tp != 0 || H <= 0 || H % global_tp != 0) return SP_ERR_INVALID_ARG;
   if (elem_bytes != 1 && elem_bytes != 2 && elem_bytes != 4 && elem_bytes != 8)
     return SP_ERR_INVALID_ARG;
+  if (N > kMaxBufferBytes / H / elem_bytes) return SP_ERR_INVALID_ARG;
   if (N == 0) return SP_OK;
   if (!x || !y) return SP_ERR_INVALID_ARG;
   const int64_t bytes = N * H * elem_bytes;

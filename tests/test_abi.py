@@ -142,6 +142,11 @@ CASES = [
     ({"out": A * 11 + 4}, "SP_ERR_ALIGNMENT"),
     ({"residual": A * 8 + 2, "residual_out": A * 13}, "SP_ERR_ALIGNMENT"),
     ({"H": 1 << 16}, "SP_ERR_UNSUPPORTED"),
+    # the partials would exceed 2^62 bytes (4 x T_pad x H x 2): a shape error, checked before
+    # any size is computed from the shapes (so nothing overflows int64), and before max H
+    ({"T_pad": (1 << 53) + 4, "T_valid": 0}, "SP_ERR_INVALID_ARG"),
+    ({"T_pad": 1 << 61, "T_valid": 0}, "SP_ERR_INVALID_ARG"),
+    ({"T_pad": 1 << 50, "T_valid": 0, "H": 1 << 16}, "SP_ERR_INVALID_ARG"),
 ]
 
 
@@ -239,6 +244,7 @@ FC2_CASES = [
     (dict(y=A * 64 + 8), "SP_ERR_ALIGNMENT"),
     (dict(H=8 * 4), "SP_ERR_ALIGNMENT"),               # 4 bf16 per slice = 8 bytes
     (dict(N=0, x=None, y=None), "SP_OK"),
+    (dict(N=1 << 56), "SP_ERR_INVALID_ARG"),           # x would exceed 2^62 bytes
 ]
 
 
