@@ -145,14 +145,30 @@ sp_status sp_check_args(const void* partials, int tp, int64_t T_pad, int64_t T_v
  *                  SP_ERR_INVALID_ARG; any other value SP_ERR_UNSUPPORTED.
  *   host_buffers   0: every tensor is in device memory; 1: tensors are in page-locked host memory
  *                  (or device memory) and are read/written across the host link (zero-copy).
+ *   schedule       how rows reach CTAs; the results are the same bytes either way.
+ *                  SP_SCHEDULE_STATIC: CTA b takes rows b, b + grid, b + 2*grid, ...
+ *                  SP_SCHEDULE_DYNAMIC: CTA b takes row b, then claims further rows from a row
+ *                  counter of the call's stream, so CTAs that get more memory bandwidth take more
+ *                  rows (applies to the staged kernel, the one device-buffer calls use).
+ *                  SP_SCHEDULE_AUTO (the default): dynamic when the staged kernel gives every CTA
+ *                  at least 10 rows, static otherwise.
+ *                  The counters are a fixed table in the library's device memory (no allocation):
+ *                  one slot per stream (told apart by cudaStreamGetId), reset by each call's last
+ *                  CTA, so calls on one stream reuse it in stream order and calls on different
+ *                  streams never share one. A call falls back to the static schedule while its
+ *                  stream is being captured into a CUDA graph (a replay may run beside calls on
+ *                  the capturing stream) and when all slots are taken. Any other value is
+ *                  SP_ERR_UNSUPPORTED.
  */
 enum { SP_SCALES_ROW_MAJOR = 0, SP_SCALES_SWIZZLED_128X4 = 1 };
+enum { SP_SCHEDULE_AUTO = 0, SP_SCHEDULE_STATIC = 1, SP_SCHEDULE_DYNAMIC = 2 };
 
 typedef struct sp_fused_options {
   float partial_scale;
   const void* addend;
   int scale_layout;
   int host_buffers;
+  int schedule;
 } sp_fused_options;
 
 void sp_options_init(sp_fused_options* options /* host, out */);

@@ -47,9 +47,13 @@ class SpError(RuntimeError):
 
 class Options(ctypes.Structure):
     """sp_fused_options: partial_scale, addend (device address or None), scale_layout,
-    host_buffers."""
+    host_buffers, schedule."""
     _fields_ = [("partial_scale", ctypes.c_float), ("addend", ctypes.c_void_p),
-                ("scale_layout", ctypes.c_int), ("host_buffers", ctypes.c_int)]
+                ("scale_layout", ctypes.c_int), ("host_buffers", ctypes.c_int),
+                ("schedule", ctypes.c_int)]
+
+
+SCHEDULES = {"auto": 0, "static": 1, "dynamic": 2}
 
 
 class LaunchConfig(ctypes.Structure):
@@ -172,15 +176,16 @@ def sp_fused_reduce_norm(partials, weight, out, residual_out, *, residual=None, 
 
 
 def sp_options_init(*, partial_scale: float = 1.0, addend=None, scale_layout: int = 0,
-                    host_buffers: bool = False) -> Options:
+                    host_buffers: bool = False, schedule="auto") -> Options:
     """An sp_fused_options initialised by the library, then set from the keywords (``addend`` is a
-    tensor or None)."""
+    tensor or None; ``schedule`` is "auto", "static", "dynamic" or the enum value)."""
     o = Options()
     load_library().sp_options_init(ctypes.byref(o))
     o.partial_scale = partial_scale
     o.addend = _ptr(addend)
     o.scale_layout = scale_layout
     o.host_buffers = 1 if host_buffers else 0
+    o.schedule = SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
     return o
 
 

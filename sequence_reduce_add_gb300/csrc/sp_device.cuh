@@ -46,6 +46,7 @@ struct Params {
   int seg_stride;             // staged kernel: bytes between ring stages (2H rounded up to 128)
   int wb_offset;              // staged kernel: byte offset of the weight/bias copy [2][H] bf16
   int ring_offset;            // staged kernel: byte offset of the ring in dynamic shared memory
+  int counter_slot;           // dynamic schedule: row counter slot of the launch's stream
 };
 
 // Per-warp slot of the row reduction: sum of squares, max |h*w| and an abort vote.

@@ -13,6 +13,11 @@
 //             consumer warps add the segments that have landed. The ring runs ahead across rows,
 //             so HBM stays busy through each row's reduction and epilogue, and the bytes in flight
 //             per SM are set by the ring depth rather than by registers.
+//             Rows go to CTAs either statically (CTA b takes rows b, b + grid, ...) or, in the
+//             dynamic variant, as claimed: CTA b starts with row b and then claims rows from a
+//             per-stream counter one row ahead, so CTAs that get more bandwidth take more rows and
+//             all finish within about one row of each other. The producer passes each row's index
+//             to the consumers beside the row's first ring stage.
 //   k_direct  The consumer threads load their vectors of every segment straight into registers
 //             with 128-bit non-coherent loads, four partials at a time.
 #pragma once
@@ -24,8 +29,14 @@ namespace spk {
 constexpr int kMaxConsumerThreads = 512;  // 16 warps
 constexpr int kProducerThreads = 32;
 
+// Row counters of the dynamic schedule: slot i is [next claim, CTAs done]. A launch uses the slot
+// of its stream; its last CTA to finish claiming sets both words back to zero, so the next launch
+// on that stream (which starts claiming only after this one has completed) finds a zeroed slot.
+constexpr int kRowCounterSlots = 256;
+__device__ unsigned int g_row_counters[2 * kRowCounterSlots];
+
 // ----------------------------------------------------------------------------------- staged
-template <int kVec, int kMode>
+template <int kVec, int kMode, bool kDynamic>
 __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
     k_staged(const Params p) {
   extern __shared__ __align__(128) unsigned char smem[];
@@ -33,6 +44,7 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
   uint64_t* empty = full + p.stages;
   RedSlot* slots = reinterpret_cast<RedSlot*>(empty + p.stages);
   int* abort_flag = reinterpret_cast<int*>(slots + 64);
+  int64_t* row_ids = reinterpret_cast<int64_t*>(abort_flag + 4);  // [stages], dynamic schedule
   unsigned char* ring = smem + p.ring_offset;
 
   const int tid = threadIdx.x;
@@ -75,23 +87,57 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
     uint32_t phase = 0;
     int64_t issued = 0;
     bool aborted = false;
-    for (int64_t t = blockIdx.x; t < p.T_valid && !aborted; t += gridDim.x) {
-      for (int seg = 0; seg < nseg; ++seg) {
-        const uint16_t* src = segment(t, seg);
-        if (!mbar_wait_bounded(smem_addr(empty + stage), phase ^ 1u, abort_flag)) {
-          if (!*static_cast<volatile int*>(abort_flag)) atomicOr(&g_error_flags, kErrWaitTimeout);
-          *static_cast<volatile int*>(abort_flag) = 1;
-          aborted = true;
-          break;
+    if constexpr (!kDynamic) {
+      for (int64_t t = blockIdx.x; t < p.T_valid && !aborted; t += gridDim.x) {
+        for (int seg = 0; seg < nseg; ++seg) {
+          const uint16_t* src = segment(t, seg);
+          if (!mbar_wait_bounded(smem_addr(empty + stage), phase ^ 1u, abort_flag)) {
+            if (!*static_cast<volatile int*>(abort_flag)) atomicOr(&g_error_flags, kErrWaitTimeout);
+            *static_cast<volatile int*>(abort_flag) = 1;
+            aborted = true;
+            break;
+          }
+          const uint32_t bar = smem_addr(full + stage);
+          mbar_arrive_expect_tx(bar, seg_bytes);
+          bulk_g2s(smem_addr(ring + stage * p.seg_stride), src, seg_bytes, bar, policy);
+          ++issued;
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
-        const uint32_t bar = smem_addr(full + stage);
-        mbar_arrive_expect_tx(bar, seg_bytes);
-        bulk_g2s(smem_addr(ring + stage * p.seg_stride), src, seg_bytes, bar, policy);
-        ++issued;
-        if (++stage == p.stages) {
-          stage = 0;
-          phase ^= 1u;
+      }
+    } else {
+      // Every row, padding rows included, takes one ring stage for its index (a padding row and
+      // the final -1 take it alone: the producer completes that stage's phase by arriving).
+      unsigned int* counter = g_row_counters + 2 * p.counter_slot;
+      int64_t next = blockIdx.x;
+      for (;;) {
+        const int64_t t = next < p.rows_total ? next : -1;
+        if (t >= 0) next = static_cast<int64_t>(gridDim.x) + atomicAdd(counter, 1u);
+        for (int seg = 0; seg < (t >= 0 && t < p.T_valid ? nseg : 1); ++seg) {
+          if (!mbar_wait_bounded(smem_addr(empty + stage), phase ^ 1u, abort_flag)) {
+            if (!*static_cast<volatile int*>(abort_flag)) atomicOr(&g_error_flags, kErrWaitTimeout);
+            *static_cast<volatile int*>(abort_flag) = 1;
+            aborted = true;
+            break;
+          }
+          const uint32_t bar = smem_addr(full + stage);
+          if (seg == 0) row_ids[stage] = t;
+          if (t >= 0 && t < p.T_valid) {
+            mbar_arrive_expect_tx(bar, seg_bytes);
+            bulk_g2s(smem_addr(ring + stage * p.seg_stride), segment(t, seg), seg_bytes, bar,
+                     policy);
+          } else {
+            mbar_arrive(bar);
+          }
+          ++issued;
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
         }
+        if (aborted || t < 0) break;
       }
     }
     // Let every copy still in flight land before this CTA can exit: wait for the last issued
@@ -102,6 +148,16 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
       const uint32_t par = static_cast<uint32_t>((last / p.stages) & 1);
       if (!mbar_wait_bounded(smem_addr(full + s), par, nullptr))
         atomicOr(&g_error_flags, kErrWaitTimeout);
+    }
+    if constexpr (kDynamic) {
+      // This CTA claims no more rows; the last CTA of the launch to get here resets the slot.
+      unsigned int* counter = g_row_counters + 2 * p.counter_slot;
+      __threadfence();
+      if (atomicAdd(counter + 1, 1u) == gridDim.x - 1) {
+        counter[0] = 0u;
+        counter[1] = 0u;
+        __threadfence();
+      }
     }
     return;
   }
@@ -130,10 +186,40 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
   int stage = 0;
   uint32_t phase = 0;
   int parity = 0;
-  for (int64_t t = blockIdx.x; t < p.rows_total; t += gridDim.x) {
-    if (t >= p.T_valid) {
-      zero_row<kVec, kMode>(p, t, c);
-      continue;
+  for (int64_t t_static = blockIdx.x;; t_static += gridDim.x) {
+    int64_t t = t_static;
+    if constexpr (!kDynamic) {
+      if (t >= p.rows_total) break;
+      if (t >= p.T_valid) {
+        zero_row<kVec, kMode>(p, t, c);
+        continue;
+      }
+    } else {
+      // The row's index sits beside its first stage. A warp acts on the wait only as a whole; a
+      // warp whose wait ran out still passes the row barrier (voting to stop), so all consumer
+      // warps pass the same barriers.
+      const bool landed = mbar_wait_bounded(smem_addr(full + stage), phase, abort_flag);
+      if (!__all_sync(0xFFFFFFFFu, landed)) {
+        if (lane == 0) {
+          if (!*static_cast<volatile int*>(abort_flag)) atomicOr(&g_error_flags, kErrWaitTimeout);
+          *static_cast<volatile int*>(abort_flag) = 1;
+        }
+        int ignored = 0;
+        row_reduce<false>(0.0f, 0.0f, 1, slots, parity, nc, &ignored);
+        break;
+      }
+      t = row_ids[stage];
+      if (t < 0) break;
+      if (t >= p.T_valid) {
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_addr(empty + stage));
+        if (++stage == p.stages) {
+          stage = 0;
+          phase ^= 1u;
+        }
+        zero_row<kVec, kMode>(p, t, c);
+        continue;
+      }
     }
     // The accumulator starts from the bias (zero without one), which keeps that load off the
     // row epilogue's critical path; with a partial scale the bias joins after the scaling.

@@ -91,7 +91,8 @@ def run_gpu_host(inp: dict, *, fill: int = 0xA5, stream=None, partial_scale: flo
 
 
 def run_gpu(inp: dict, *, config: dict | None = None, fill: int = 0xA5, inplace: bool = False,
-            stream=None, partial_scale: float = 1.0, scale_layout: int = 0) -> dict:
+            stream=None, partial_scale: float = 1.0, scale_layout: int = 0,
+            schedule: str = "auto") -> dict:
     """Run the library once on inputs ``inp`` (device tensors from synth.make_inputs) into
     guard-banded outputs pre-filled with ``fill``; returns host numpy results."""
     dev = inp["partials"].device
@@ -121,10 +122,11 @@ def run_gpu(inp: dict, *, config: dict | None = None, fill: int = 0xA5, inplace:
         scale_t = torch.tensor([inp["scale"]], dtype=torch.float32, device=dev)
     kw = dict(residual=residual, bias=inp["bias"], eps=inp["eps"], quant_mode=mode, scale=scale_t,
               out_scales=sc, T_valid=inp["T_valid"], stream=stream)
-    if partial_scale != 1.0 or inp.get("addend") is not None or scale_layout != 0:
+    if (partial_scale != 1.0 or inp.get("addend") is not None or scale_layout != 0
+            or schedule != "auto"):
         assert config is None
         opts = sp.sp_options_init(partial_scale=partial_scale, addend=inp.get("addend"),
-                                  scale_layout=scale_layout)
+                                  scale_layout=scale_layout, schedule=schedule)
         sp.sp_fused_reduce_norm_ex(opts, inp["partials"], inp["weight"], out, res_out, **kw)
     elif config is None:
         sp.sp_fused_reduce_norm(inp["partials"], inp["weight"], out, res_out, **kw)

@@ -204,6 +204,10 @@ OPTION_CASES = [
     (dict(scale_layout=1), {"quant_mode": "nvfp4", "scale": A * 14,
                             "out_scales": A * 13 - 256}, "SP_ERR_INVALID_ARG"),
     (dict(host_buffers=2), {}, "SP_ERR_UNSUPPORTED"),
+    (dict(schedule=1), {}, "SP_OK"),
+    (dict(schedule=2), {}, "SP_OK"),
+    (dict(schedule=3), {}, "SP_ERR_UNSUPPORTED"),
+    (dict(schedule=-1), {}, "SP_ERR_UNSUPPORTED"),
     (dict(addend=A * 20), {"T_pad": 18}, "SP_ERR_INVALID_ARG"),     # shape rule first
 ]
 
@@ -213,6 +217,7 @@ def test_option_checks(lib, opt, kw, want):
     o = sp.Options()
     lib.sp_options_init(ctypes.byref(o))
     assert o.partial_scale == 1.0 and o.addend is None and o.scale_layout == 0
+    assert o.host_buffers == 0 and o.schedule == 0  # SP_SCHEDULE_AUTO
     for k, v in opt.items():
         setattr(o, k, v)
     a = {**_base(), **kw}

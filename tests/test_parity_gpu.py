@@ -23,9 +23,9 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
 
 
-def _check(inp, config=None, inplace=False, stream=None):
-    a = run_gpu(inp, config=config, fill=0xA5, inplace=inplace, stream=stream)
-    b = run_gpu(inp, config=config, fill=0x5A, inplace=inplace, stream=stream)
+def _check(inp, config=None, inplace=False, stream=None, schedule="auto"):
+    a = run_gpu(inp, config=config, fill=0xA5, inplace=inplace, stream=stream, schedule=schedule)
+    b = run_gpu(inp, config=config, fill=0x5A, inplace=inplace, stream=stream, schedule=schedule)
     for k in ("out", "out_scales", "residual_out"):
         if a[k] is not None:
             assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), \
@@ -315,3 +315,141 @@ def test_two_streams_concurrently():
     torch.cuda.synchronize()
     compare(_host(oa), run_oracle(a), a)
     compare(_host(ob), run_oracle(b), b)
+
+
+# ------------------------------------------------------------------------- row schedules
+def _call_ex(inp, outs, stream=None, schedule="auto"):
+    sc = None if inp["scale"] is None else torch.tensor([inp["scale"]], device=DEV)
+    sp.sp_fused_reduce_norm_ex(sp.sp_options_init(schedule=schedule), inp["partials"],
+                               inp["weight"], outs["out"], outs["residual_out"],
+                               residual=inp["residual"], bias=inp["bias"], eps=inp["eps"],
+                               quant_mode=inp["mode"], scale=sc, out_scales=outs["out_scales"],
+                               T_valid=inp["T_valid"], stream=stream)
+
+
+@pytest.mark.parametrize("wi", range(1, 6))
+@pytest.mark.parametrize("schedule", ["static", "dynamic"])
+def test_schedule_forced(wi, schedule):
+    """Each row schedule on every workload's shape (330 rows, a ragged padded tail). Each case
+    runs twice on one stream, so the second dynamic call also checks that the first left its
+    row counter at zero."""
+    assert _check(_small(synth.workload(wi)), schedule=schedule)
+
+
+@pytest.mark.parametrize("wi,rows", [(2, 4096), (3, 1024), (4, 1024), (5, 2048)])
+def test_schedules_give_identical_bytes(wi, rows):
+    """Static and dynamic schedules compute every row the same way: byte-identical outputs."""
+    inp = _small(synth.workload(wi), rows=rows)
+    a = run_gpu(inp, schedule="static")
+    b = run_gpu(inp, schedule="dynamic")
+    for k in ("out", "out_scales", "residual_out"):
+        if a[k] is not None:
+            assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+
+
+@pytest.mark.parametrize("mode", ["none", "fp8_static", "fp8_per_token", "nvfp4"])
+def test_dynamic_schedule_with_options(mode):
+    """Dynamic rows with a partial scale, an addend and (NVFP4) the swizzled scale layout, whose
+    128-row padding adds rows beyond T_pad."""
+    w = dict(synth.workload(3), mode=mode, scale=0.05 if mode == "fp8_static" else None)
+    inp = synth.make_inputs(w, device=DEV, T_pad=200, T_valid=197, H=5120, with_addend=True)
+    layout = 1 if mode == "nvfp4" else 0
+    a = run_gpu(inp, fill=0xA5, partial_scale=0.5, scale_layout=layout, schedule="dynamic")
+    b = run_gpu(inp, fill=0x5A, partial_scale=0.5, scale_layout=layout, schedule="dynamic")
+    for k in ("out", "out_scales", "residual_out"):
+        if a[k] is not None:
+            assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+    compare(a, run_oracle(inp, partial_scale=0.5, scale_layout=layout), inp)
+
+
+def test_dynamic_schedule_on_two_streams_concurrently():
+    """Dynamic calls on two streams at once use different row counters: both results correct."""
+    w = synth.workload(3)
+    a = _small(w, rows=1024)
+    b = synth.make_inputs(w, device=DEV, T_pad=a["T_pad"], T_valid=a["T_valid"] - 4,
+                          seed=a["seed"] + 5)
+    oa = sp.allocate_outputs(a["T_pad"], a["H"], a["mode"], DEV)
+    ob = sp.allocate_outputs(b["T_pad"], b["H"], b["mode"], DEV)
+    sa, sb = torch.cuda.Stream(device=DEV), torch.cuda.Stream(device=DEV)
+    torch.cuda.synchronize()
+    for _ in range(50):
+        _call_ex(a, oa, stream=sa, schedule="dynamic")
+        _call_ex(b, ob, stream=sb, schedule="dynamic")
+    torch.cuda.synchronize()
+    compare(_host(oa), run_oracle(a), a)
+    compare(_host(ob), run_oracle(b), b)
+
+
+def test_dynamic_schedule_with_more_streams_than_counter_slots():
+    """Streams beyond the counter table fall back to the static schedule: still correct."""
+    w = synth.workload(2)
+    inp = _small(w, rows=64)
+    outs = [sp.allocate_outputs(inp["T_pad"], inp["H"], inp["mode"], DEV) for _ in range(300)]
+    # 300 distinct CUDA streams (torch's stream pool would hand out the same few again)
+    raw = [torch.cuda.ExternalStream(_new_raw_stream()) for _ in range(300)]
+    torch.cuda.synchronize()
+    for o, st in zip(outs, raw):
+        _call_ex(inp, o, stream=st, schedule="dynamic")
+    torch.cuda.synchronize()
+    ref = run_oracle(inp)
+    for o in (outs[0], outs[150], outs[299]):
+        compare(_host(o), ref, inp)
+    first = _host(outs[0])
+    for o in outs[1:]:
+        h = _host(o)
+        for k in ("out", "residual_out"):
+            assert np.array_equal(h[k].view(np.uint8), first[k].view(np.uint8))
+    for st in raw:
+        _destroy_raw_stream(st.cuda_stream)
+
+
+def _cudart():
+    import ctypes
+    for name in ("libcudart.so", "libcudart.so.13", "libcudart.so.12"):
+        try:
+            return ctypes.CDLL(name)
+        except OSError:
+            continue
+    import glob
+    import os
+    for path in glob.glob(os.path.join(os.path.dirname(torch.__file__), "lib", "libcudart*.so*")):
+        return ctypes.CDLL(path)
+    pytest.skip("no CUDA runtime library to create raw streams")
+
+
+def _new_raw_stream() -> int:
+    import ctypes
+    rt = _cudart()
+    h = ctypes.c_void_p()
+    assert rt.cudaStreamCreateWithFlags(ctypes.byref(h), 1) == 0  # non-blocking
+    return h.value
+
+
+def _destroy_raw_stream(h: int) -> None:
+    import ctypes
+    _cudart().cudaStreamDestroy(ctypes.c_void_p(h))
+
+
+def test_dynamic_schedule_requested_under_graph_capture():
+    """A dynamic call captured into a CUDA graph runs with the static schedule and replays
+    correctly on refilled inputs."""
+    w = synth.workload(4)
+    inp = _small(w, rows=1024)
+    outs = sp.allocate_outputs(inp["T_pad"], inp["H"], inp["mode"], DEV)
+    s = torch.cuda.Stream(device=DEV)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        _call_ex(inp, outs, schedule="dynamic")
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        _call_ex(inp, outs, schedule="dynamic")
+    fresh = synth.make_inputs(w, device=DEV, T_pad=inp["T_pad"], T_valid=inp["T_valid"],
+                              seed=inp["seed"] + 91)
+    for k in ("partials", "residual", "weight", "bias"):
+        inp[k].copy_(fresh[k])
+    torch.cuda.synchronize()
+    g.replay()
+    with torch.cuda.stream(s):
+        _call_ex(inp, outs, schedule="dynamic")  # the capturing stream, outside the graph
+    torch.cuda.synchronize()
+    compare(_host(outs), run_oracle(fresh), fresh)

@@ -1,5 +1,5 @@
 """GPU parity on seeded random problems: shapes, modes, optional inputs, options and launch
-configurations drawn together, so that combinations the hand-picked cases do not list are
+configurations and row schedules drawn together, so that combinations the hand-picked cases do not list are
 covered too. Each problem is compared with the oracle element by element under the tolerances
 of parity_util, after two runs into differently pre-filled, guard-banded outputs. Random
 FlashComm2 reorganisations are compared byte for byte.
@@ -40,12 +40,15 @@ def _draw(i: int) -> dict:
              outliers=r.choice([0, 0, min(H, 3)]),
              with_residual=r.random() < 0.8, with_bias=r.random() < 0.7,
              with_addend=r.random() < 0.25, inplace=False, config=None,
-             partial_scale=1.0, scale_layout=0, seed=1000 + i)
+             partial_scale=1.0, scale_layout=0, schedule="auto", seed=1000 + i)
     if r.random() < 0.25:
         p["partial_scale"] = r.choice([0.5, 1.0 / 3.0, -2.0, 0.125])
     if mode == "nvfp4" and r.random() < 0.4:
         p["scale_layout"] = 1
-    options = p["with_addend"] or p["partial_scale"] != 1.0 or p["scale_layout"] != 0
+    if r.random() < 0.3:
+        p["schedule"] = r.choice(["static", "dynamic"])
+    options = (p["with_addend"] or p["partial_scale"] != 1.0 or p["scale_layout"] != 0
+               or p["schedule"] != "auto")
     if not options:
         if p["with_residual"] and r.random() < 0.2:
             p["inplace"] = True
@@ -73,7 +76,7 @@ def test_random_problem(i):
     p = _draw(i)
     inp = _inputs(p)
     kw = dict(config=p["config"], inplace=p["inplace"], partial_scale=p["partial_scale"],
-              scale_layout=p["scale_layout"])
+              scale_layout=p["scale_layout"], schedule=p["schedule"])
     try:
         a = run_gpu(inp, fill=0xA5, **kw)
     except sp.SpError as e:
@@ -102,6 +105,7 @@ def test_draws_cover_every_mode_and_option():
     assert any(p["config"] and p["config"]["kernel"] == 1 for p in ps)
     assert any(not p["with_residual"] for p in ps) and any(not p["with_bias"] for p in ps)
     assert any(p["T_valid"] < p["T_pad"] for p in ps)
+    assert {p["schedule"] for p in ps} == {"auto", "static", "dynamic"}
 
 
 def _draw_fc2(i: int) -> dict:
