@@ -295,8 +295,9 @@ class OracleRunner:
         self.buffers = None
         self.next_row = 0
 
-    def run(self, nrows: int) -> tuple[float, int]:
-        """Compute `nrows` valid rows (cycling through the workload); returns (seconds, bytes)."""
+    def run(self, nrows: int, threads: int | None = None) -> tuple[float, int]:
+        """Compute `nrows` valid rows (cycling through the workload) on `threads` threads (default:
+        all cores); returns (seconds, bytes)."""
         Tv = self.w["T_valid"]
         nrows = max(1, min(nrows, Tv))
         if self.next_row + nrows > Tv:
@@ -306,38 +307,48 @@ class OracleRunner:
         t0 = time.perf_counter()
         r = self.oracle.fused_reduce_norm(self.parts, self.res, self.wt, self.bs, 1e-6,
                                           self.w["mode"], self.scale, Tv, rows=rows,
-                                          threads=min(self.cores, nrows), buffers=self.buffers)
+                                          threads=min(threads or self.cores, nrows),
+                                          buffers=self.buffers)
         dt = time.perf_counter() - t0
         assert r["status"] == 0
         self.buffers = r
         tp, _, H = self.parts.shape
         return dt, algorithmic_bytes(tp, nrows, nrows, H, self.w["mode"], self.res is not None)
 
-    def rows_for(self, seconds: float) -> int:
+    def rows_for(self, seconds: float, threads: int | None = None) -> int:
         """Rows that take about `seconds`, from a probe of 8 rows per thread."""
-        probe = min(self.w["T_valid"], 8 * self.cores)
-        self.run(probe)  # warm caches and the library
-        dt, _ = self.run(probe)
+        probe = min(self.w["T_valid"], 8 * (threads or self.cores))
+        self.run(probe, threads)  # warm caches and the library
+        dt, _ = self.run(probe, threads)
         return max(1, int(probe * seconds / max(dt, 1e-6)))
 
 
-def cpu_baseline(w: dict, host_in: dict, target_s: float = 12.0) -> dict:
+def cpu_baseline(w: dict, host_in: dict, target_s: float = 12.0,
+                 single_thread_s: float = 3.0) -> dict:
     """The oracle as it stands, on all host cores, over a bounded sample of about `target_s`
     seconds: consecutive valid rows of the workload, wrapping around when the sample is larger
-    than the workload."""
+    than the workload. Beside it, the same on one thread over about `single_thread_s` seconds."""
     runner = OracleRunner(w, host_in)
-    want = runner.rows_for(target_s)
-    runner.next_row = 0
-    done, secs, nbytes = 0, 0.0, 0
-    while done < want:
-        n = min(w["T_valid"], want - done)
-        dt, b = runner.run(n)
-        done, secs, nbytes = done + n, secs + dt, nbytes + b
+
+    def sample(seconds: float, threads: int | None) -> tuple[int, float, int]:
+        want = runner.rows_for(seconds, threads)
+        runner.next_row = 0
+        done, secs, nbytes = 0, 0.0, 0
+        while done < want:
+            n = min(w["T_valid"], want - done)
+            dt, b = runner.run(n, threads)
+            done, secs, nbytes = done + n, secs + dt, nbytes + b
+        return done, secs, nbytes
+
+    done, secs, nbytes = sample(target_s, None)
+    d1, s1, b1 = sample(single_thread_s, 1)
     return {"value": nbytes / secs / 1e9, "unit": "GB/s", "cores": runner.cores, "kind": "oracle",
             "sample": f"{done} valid rows ({done / w['T_valid']:.2f} passes over the workload's "
                       f"{w['T_valid']} rows, {nbytes / 1e6:.0f} MB algorithmic), "
                       f"{runner.cores} threads, {secs:.1f} s",
-            "mtokens_per_s": done / secs / 1e6}
+            "mtokens_per_s": done / secs / 1e6,
+            "single_thread": {"value": b1 / s1 / 1e9, "unit": "GB/s",
+                              "sample": f"{d1} valid rows, 1 thread, {s1:.1f} s"}}
 
 
 def max_over_ranks(value: float, device) -> float:
@@ -411,6 +422,7 @@ def run_ours(args) -> None:
     kernel_ms = ms_per_step
     _, isolated = time_kernel_loop(lib, problems, min(args.steps, 300), stream, True)
     isolated_ms = float(np.mean(isolated))
+    isolated_median_ms, isolated_min_ms = float(np.median(isolated)), float(np.min(isolated))
     peak, peak_kind = measured_peak()
     achieved = one / (kernel_ms / 1e3) / 1e9
 
@@ -452,6 +464,8 @@ def run_ours(args) -> None:
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": ncu_traffic(w["name"], cfg), "kernel_ms": round(kernel_ms, 6),
                      "isolated_launch_ms": round(isolated_ms, 6),
+                     "isolated_launch_ms_median": round(isolated_median_ms, 6),
+                     "isolated_launch_ms_min": round(isolated_min_ms, 6),
                      "isolated_frac": round(one / (isolated_ms / 1e3) / 1e9 / peak, 4),
                      "kernel": "k_staged" if cfg["kernel"] == 0 else "k_direct"},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
