@@ -428,8 +428,8 @@ extern "C" {
 
 sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
                            sp_launch_config* config) {
-  (void)tp;
-  if (!config || H <= 0 || H % 8 != 0 || T_pad < 0 || T_pad > kMaxBufferBytes / (2 * H))
+  if (!config || tp < 1 || H <= 0 || H % 8 != 0 || T_pad < 0 ||
+      T_pad > kMaxBufferBytes / (2 * H) / tp)
     return SP_ERR_INVALID_ARG;
   if (quant_mode < SP_QUANT_NONE || quant_mode > SP_QUANT_FP8_DYNAMIC_PER_TENSOR)
     return SP_ERR_INVALID_ARG;
@@ -452,14 +452,37 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     c.kernel = SP_KERNEL_DIRECT;
     c.stages = 0;
   }
-  // Tiny problems (at most 2^20 row elements, H <= 4096) are latency-bound: every CTA does one
-  // or two rows, and the direct kernel (no ring to set up) with one vector per thread and many
-  // CTAs per SM finishes 15-30 % sooner there.
-  if (H <= 4096 && T_pad * H <= (int64_t{1} << 20)) {
+  // Small calls (decode-sized batches) are latency-bound, every CTA doing about one row. The
+  // direct kernel (no ring to set up; loads four partials at a time) is fastest while its loads
+  // fit in one wave; the staged kernel's floor grows with the row's segment count (each passes
+  // through the ring in turn), but it keeps all of a row's segments in flight with a deep ring.
+  // From a GB300 sweep of tp 2-16, H 1024-8192, T 8-4096 (call time):
+  //   H <= 4096, T <= 256: direct below ~1.5M partial elements for tp <= 4 (2M for larger tp),
+  //                        else the staged kernel at 2 CTAs/SM with as many stages as fit
+  //                        (7-27 % faster than either previous choice);
+  //   H <= 4096, T > 256:  direct while T * H <= 2^20;
+  //   4096 < H <= 8192:    direct while tp * T * H <= 2^20 (13-30 % faster at T = 8-64).
+  const int64_t elems = static_cast<int64_t>(tp) * T_pad * H;
+  bool direct = false;
+  bool deep_ring = false;
+  if (H <= 4096) {
+    if (T_pad <= 256) {
+      direct = tp <= 4 ? elems < 3 * (int64_t{1} << 19) : elems <= (int64_t{1} << 21);
+      deep_ring = !direct;
+    } else {
+      direct = T_pad * H <= (int64_t{1} << 20);
+    }
+  } else if (H <= 8192) {
+    direct = elems <= (int64_t{1} << 20);
+  }
+  if (direct) {
     c.kernel = SP_KERNEL_DIRECT;
-    c.vec_per_thread = 1;
-    c.ctas_per_sm = 16;
+    c.vec_per_thread = H <= 4096 ? 1 : 2;
+    c.ctas_per_sm = H <= 4096 ? 16 : 8;
     c.stages = 0;
+  } else if (deep_ring && c.kernel == SP_KERNEL_STAGED && max_stages(H, 2) >= c.stages) {
+    c.ctas_per_sm = 2;
+    c.stages = 0;  // as many as fit
   }
   *config = c;
   return SP_OK;

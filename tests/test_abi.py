@@ -98,6 +98,24 @@ def test_launch_selection(lib):
         sp.sp_select_launch(2, 8, sp.sp_max_hidden() + 8, "none")
 
 
+@pytest.mark.parametrize("tp,T,H,want", [
+    (2, 64, 1024, (1, 1, 16, 0)),       # tiny: direct, one vector per thread
+    (4, 64, 4096, (1, 1, 16, 0)),       # 1M partial elements, tp <= 4: direct
+    (4, 128, 4096, (0, 2, 2, 0)),       # 2M, few rows: staged, deep ring at 2 CTAs/SM
+    (8, 64, 4096, (1, 1, 16, 0)),       # 2M, tp > 4: direct
+    (16, 64, 4096, (0, 2, 2, 0)),       # 4M: deep ring
+    (8, 512, 2048, (1, 1, 16, 0)),      # T > 256: direct while T * H <= 2^20
+    (4, 32, 8192, (1, 2, 8, 0)),        # 4096 < H <= 8192: direct while tp*T*H <= 2^20
+    (8, 32, 8192, (0, 2, 2, 4)),        # 2M: the staged kernel
+    (4, 4096, 4096, (0, 2, 4, 3)),      # large: staged, CTAs/SM = 16384 / H
+    (8, 8192, 7168, (0, 2, 2, 4)),
+    (8, 16384, 5120, (0, 2, 3, 3)),
+])
+def test_launch_rule(lib, tp, T, H, want):
+    c = sp.sp_select_launch(tp, T, H, "none")
+    assert (c.kernel, c.vec_per_thread, c.ctas_per_sm, c.stages) == want
+
+
 A = 1 << 20  # fake 16-byte-aligned addresses: compared, never dereferenced
 
 
