@@ -133,11 +133,19 @@ __device__ __forceinline__ void scale8(float (&v)[8], float f) {
 
 // ---------------------------------------------------------------- conversions
 // bf16 -> fp32 is exact: the bf16 pattern is the top half of the binary32 pattern.
+__device__ __forceinline__ void add_bf16x2(uint32_t v, float& a0, float& a1) {
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "mov.b32 {lo, hi}, %2;\n\t"
+      "add.rn.f32.bf16 %0, lo, %0;\n\t"
+      "add.rn.f32.bf16 %1, hi, %1;\n\t}"
+      : "+f"(a0), "+f"(a1)
+      : "r"(v));
+}
 __device__ __forceinline__ void add_bf16x8(const uint4 v, float (&acc)[8]) {
-  add2(acc[0], acc[1], __uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u));
-  add2(acc[2], acc[3], __uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
-  add2(acc[4], acc[5], __uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u));
-  add2(acc[6], acc[7], __uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+  add_bf16x2(v.x, acc[0], acc[1]);
+  add_bf16x2(v.y, acc[2], acc[3]);
+  add_bf16x2(v.z, acc[4], acc[5]);
+  add_bf16x2(v.w, acc[6], acc[7]);
 }
 
 __device__ __forceinline__ void unpack_bf16x8(const uint4 v, float (&f)[8]) {
