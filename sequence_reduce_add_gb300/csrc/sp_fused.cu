@@ -461,10 +461,13 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   //                        else the staged kernel at 2 CTAs/SM with as many stages as fit
   //                        (7-27 % faster than either previous choice);
   //   H <= 4096, T > 256:  direct while T * H <= 2^20;
-  //   4096 < H <= 8192:    direct while tp * T * H <= 2^20 (13-30 % faster at T = 8-64).
+  //   4096 < H <= 8192:    direct while tp * T * H <= 2^20 (13-30 % faster at T = 8-64);
+  //                        for 64-128 rows, the staged kernel at one CTA per SM with every
+  //                        stage that fits (a 12-stage ring at H = 8192: 10-34 % faster).
   const int64_t elems = static_cast<int64_t>(tp) * T_pad * H;
   bool direct = false;
   bool deep_ring = false;
+  bool deep_ring_1 = false;
   if (H <= 4096) {
     if (T_pad <= 256) {
       direct = tp <= 4 ? elems < 3 * (int64_t{1} << 19) : elems <= (int64_t{1} << 21);
@@ -474,6 +477,7 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     }
   } else if (H <= 8192) {
     direct = elems <= (int64_t{1} << 20);
+    deep_ring_1 = !direct && T_pad >= 64 && T_pad <= 128;
   }
   if (direct) {
     c.kernel = SP_KERNEL_DIRECT;
@@ -483,6 +487,9 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   } else if (deep_ring && c.kernel == SP_KERNEL_STAGED && max_stages(H, 2) >= c.stages) {
     c.ctas_per_sm = 2;
     c.stages = 0;  // as many as fit
+  } else if (deep_ring_1 && c.kernel == SP_KERNEL_STAGED && max_stages(H, 1) >= c.stages) {
+    c.ctas_per_sm = 1;
+    c.stages = 0;
   }
   *config = c;
   return SP_OK;

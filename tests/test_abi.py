@@ -107,6 +107,9 @@ def test_launch_selection(lib):
     (8, 512, 2048, (1, 1, 16, 0)),      # T > 256: direct while T * H <= 2^20
     (4, 32, 8192, (1, 2, 8, 0)),        # 4096 < H <= 8192: direct while tp*T*H <= 2^20
     (8, 32, 8192, (0, 2, 2, 4)),        # 2M: the staged kernel
+    (8, 64, 8192, (0, 2, 1, 0)),        # 64-128 rows: one CTA per SM, deepest ring
+    (16, 128, 7168, (0, 2, 1, 0)),
+    (16, 256, 7168, (0, 2, 2, 4)),
     (4, 4096, 4096, (0, 2, 4, 3)),      # large: staged, CTAs/SM = 16384 / H
     (8, 8192, 7168, (0, 2, 2, 4)),
     (8, 16384, 5120, (0, 2, 3, 3)),
