@@ -453,3 +453,38 @@ def test_dynamic_schedule_requested_under_graph_capture():
         _call_ex(inp, outs, schedule="dynamic")  # the capturing stream, outside the graph
     torch.cuda.synchronize()
     compare(_host(outs), run_oracle(fresh), fresh)
+
+
+# ------------------------------------------------------------------------- non-finite inputs
+def _drop_rows(res: dict, rows) -> dict:
+    out = {}
+    for k, v in res.items():
+        if isinstance(v, np.ndarray) and v.ndim >= 1 and k in ("out", "out_scales", "residual_out", "y"):
+            out[k] = np.delete(v, rows, axis=0)
+        else:
+            out[k] = v
+    return out
+
+
+@pytest.mark.parametrize("mode", ["none", "fp8_static", "fp8_per_token", "nvfp4"])
+@pytest.mark.parametrize("schedule", ["static", "dynamic"])
+def test_non_finite_inputs_stay_in_their_row(mode, schedule):
+    """Inf and NaN in valid rows are outside the stage's contract (the pages define no such
+    inputs), but they must not leak: every other row still matches the oracle exactly as usual,
+    padding rows stay zero, and no device wait runs out."""
+    w = dict(synth.workload(3), mode=mode, scale=0.05 if mode == "fp8_static" else None)
+    inp = synth.make_inputs(w, device=DEV, T_pad=64, T_valid=61, H=1024)
+    poisoned = [3, 17, 40]
+    inp["partials"][1, 3, 5] = float("inf")
+    inp["residual"][17, 100] = float("nan")
+    inp["partials"][0, 40, 7] = float("-inf")
+    inp["partials"][2, 40, 7] = float("inf")
+    a = run_gpu(inp, fill=0xA5, schedule=schedule)
+    b = run_gpu(inp, fill=0x5A, schedule=schedule)
+    for k in ("out", "out_scales", "residual_out"):
+        if a[k] is not None:
+            assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+    ref = run_oracle(inp)
+    clean = dict(inp, T_valid=inp["T_valid"] - len(poisoned))
+    compare(_drop_rows(a, poisoned), _drop_rows(ref, poisoned), clean)
+    assert sp.sp_device_error(clear=False) == 0
