@@ -488,3 +488,31 @@ def test_non_finite_inputs_stay_in_their_row(mode, schedule):
     clean = dict(inp, T_valid=inp["T_valid"] - len(poisoned))
     compare(_drop_rows(a, poisoned), _drop_rows(ref, poisoned), clean)
     assert sp.sp_device_error(clear=False) == 0
+
+
+def test_dynamic_schedule_chained_with_other_kernels_on_one_stream():
+    """A layer loop on one stream: each call's new residual feeds the next call (in place), with
+    PyTorch kernels between the calls. Dynamic rows, so every call reuses the stream's row
+    counter right after the previous call; the final residual matches the same loop run with the
+    static schedule byte for byte."""
+    w = synth.workload(4)
+    inp = _small(w, rows=1024)
+    s = torch.cuda.Stream(device=DEV)
+    finals = []
+    for schedule in ("dynamic", "static"):
+        res = inp["residual"].clone()
+        outs = sp.allocate_outputs(inp["T_pad"], inp["H"], inp["mode"], DEV)
+        parts = inp["partials"].clone()
+        with torch.cuda.stream(s):
+            for layer in range(12):
+                opts = sp.sp_options_init(schedule=schedule)
+                sp.sp_fused_reduce_norm_ex(opts, parts, inp["weight"], outs["out"], res,
+                                           residual=res, bias=inp["bias"], eps=inp["eps"],
+                                           quant_mode=inp["mode"], out_scales=outs["out_scales"],
+                                           T_valid=inp["T_valid"], stream=s)
+                parts.mul_(0.5)  # a PyTorch kernel between two calls on the same stream
+        torch.cuda.synchronize()
+        finals.append((res.view(torch.int16).cpu().numpy(), outs["out"].cpu().numpy(),
+                       outs["out_scales"].cpu().numpy()))
+    for a, b in zip(finals[0], finals[1]):
+        assert np.array_equal(a, b)
