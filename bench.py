@@ -62,10 +62,13 @@ KERNEL_SOURCES = ("sp_device.cuh", "sp_kernels.cuh")  # the device code of every
 
 
 def kernel_source_hash() -> str:
+    """Hash of the device code the fused kernels compile from: comments and blank lines are left
+    out, so only a change to the code itself marks recorded ncu counters as stale."""
     h = hashlib.sha256()
     for rel in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, "sequence_reduce_add_gb300", "csrc", rel), "rb") as f:
-            h.update(rel.encode() + f.read())
+        with open(os.path.join(ROOT, "sequence_reduce_add_gb300", "csrc", rel)) as f:
+            code = [line.split("//", 1)[0].rstrip() for line in f]
+        h.update(rel.encode() + "\n".join(line for line in code if line).encode())
     return h.hexdigest()[:16]
 
 

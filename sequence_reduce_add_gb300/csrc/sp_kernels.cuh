@@ -1,8 +1,8 @@
 // sp_kernels.cuh — the two kernels of the fused stage. Both map one token row at a time to one
 // CTA (rows are independent: RMSNorm and every scale kind used here are per token), walk rows
-// with a grid stride in token order, and make a single pass over HBM: every partial, residual
-// and output byte of a valid row is read or written exactly once; padding rows are written as
-// zeros without any read.
+// in token order (a grid stride, or claimed in the staged kernel's dynamic variant below), and
+// make a single pass over HBM: every partial, residual and output byte of a valid row is read
+// or written exactly once; padding rows are written as zeros without any read.
 //
 // Thread c of the CTA's consumer threads owns 16-byte vectors v = c + k*nthreads (k < VEC) of
 // the row, i.e. 8*VEC columns, held as fp32 accumulators in registers for the whole row.
