@@ -464,7 +464,8 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   //   H <= 4096, T <= 256: direct below ~1.5M partial elements for tp <= 4 (2M for larger tp),
   //                        else the staged kernel at 2 CTAs/SM with as many stages as fit
   //                        (7-27 % faster than either previous choice);
-  //   H <= 4096, T > 256:  direct while T * H <= 2^20;
+  //   H <= 4096, T > 256:  direct while T * H <= 2^20 (2^22 for H <= 1024, where a row's
+  //                        2 KB segments leave the ring little to hide: 10-35 % faster);
   //   4096 < H <= 8192:    direct while tp * T * H <= 2^20 (13-30 % faster at T = 8-64);
   //                        for 64-128 rows, the staged kernel at one CTA per SM with every
   //                        stage that fits (a 12-stage ring at H = 8192: 10-34 % faster).
@@ -477,7 +478,7 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
       direct = tp <= 4 ? elems < 3 * (int64_t{1} << 19) : elems <= (int64_t{1} << 21);
       deep_ring = !direct;
     } else {
-      direct = T_pad * H <= (int64_t{1} << 20);
+      direct = T_pad * H <= (int64_t{1} << (H <= 1024 ? 22 : 20));
     }
   } else if (H <= 8192) {
     direct = elems <= (int64_t{1} << 20);

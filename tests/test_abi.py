@@ -105,6 +105,8 @@ def test_launch_selection(lib):
     (8, 64, 4096, (1, 1, 16, 0)),       # 2M, tp > 4: direct
     (16, 64, 4096, (0, 2, 2, 0)),       # 4M: deep ring
     (8, 512, 2048, (1, 1, 16, 0)),      # T > 256: direct while T * H <= 2^20
+    (4, 4096, 1024, (1, 1, 16, 0)),     # ... 2^22 for H <= 1024
+    (4, 8192, 1024, (0, 2, 16, 4)),
     (4, 32, 8192, (1, 2, 8, 0)),        # 4096 < H <= 8192: direct while tp*T*H <= 2^20
     (8, 32, 8192, (0, 2, 2, 4)),        # 2M: the staged kernel
     (8, 64, 8192, (0, 2, 1, 0)),        # 64-128 rows: one CTA per SM, deepest ring
