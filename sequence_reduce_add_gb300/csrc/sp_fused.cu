@@ -121,7 +121,8 @@ constexpr int kFc2CtasPerSm = 3;
 constexpr int kSmemReservedPerCta = 1024;
 
 struct DeviceInfo {
-  int sms = 0;
+  int id = 0;
+  std::atomic<int> sms{0};
   std::atomic<bool> staged_attr_set[3][4][2] = {};
   std::atomic<bool> fc2_attr_set{false};
   // Row counter slots of the dynamic schedule: slot i belongs to the stream with id slot_stream[i].
@@ -135,13 +136,16 @@ std::mutex g_devices_mutex;
 sp_status device_info(DeviceInfo** info) {
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SP_ERR_CUDA;
-  std::lock_guard<std::mutex> lock(g_devices_mutex);
   DeviceInfo& d = g_devices[dev];
-  if (d.sms == 0) {
-    int sms = 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
-      return SP_ERR_CUDA;
-    d.sms = sms;
+  if (d.sms.load(std::memory_order_acquire) == 0) {  // first call on this device
+    std::lock_guard<std::mutex> lock(g_devices_mutex);
+    if (d.sms.load(std::memory_order_relaxed) == 0) {
+      int sms = 0;
+      if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        return SP_ERR_CUDA;
+      d.id = dev;
+      d.sms.store(sms, std::memory_order_release);
+    }
   }
   *info = &d;
   return SP_OK;
@@ -223,24 +227,37 @@ int g_occ_values[kOccupancySlots];
 int g_occ_used = 0;
 std::mutex g_occ_mutex;
 
+// The calling thread's last lookup, checked before the shared table: a thread that keeps
+// launching the same shape takes no lock.
+struct LastOccupancy {
+  const void* kernel;
+  int device, threads, smem, value;
+};
+thread_local LastOccupancy t_last_occupancy{nullptr, -1, 0, 0, 0};
+
 template <typename Kernel>
-cudaError_t resident_ctas(Kernel kernel, int threads, int smem, int* resident) {
-  int device = 0;
-  cudaError_t e = cudaGetDevice(&device);
-  if (e != cudaSuccess) return e;
+cudaError_t resident_ctas(Kernel kernel, int threads, int smem, int device, int* resident) {
   const void* k = reinterpret_cast<const void*>(kernel);
+  const LastOccupancy& last = t_last_occupancy;
+  if (last.kernel == k && last.device == device && last.threads == threads && last.smem == smem) {
+    *resident = last.value;
+    return cudaSuccess;
+  }
+  cudaError_t e = cudaSuccess;
   {
     std::lock_guard<std::mutex> lock(g_occ_mutex);
     for (int i = 0; i < g_occ_used; ++i) {
       const OccupancyKey& c = g_occ_keys[i];
       if (c.kernel == k && c.device == device && c.threads == threads && c.smem == smem) {
         *resident = g_occ_values[i];
+        t_last_occupancy = LastOccupancy{k, device, threads, smem, *resident};
         return cudaSuccess;
       }
     }
   }
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(resident, kernel, threads, smem);
   if (e != cudaSuccess) return e;
+  t_last_occupancy = LastOccupancy{k, device, threads, smem, *resident};
   std::lock_guard<std::mutex> lock(g_occ_mutex);
   if (g_occ_used < kOccupancySlots) {
     g_occ_keys[g_occ_used] = OccupancyKey{k, device, threads, smem};
@@ -254,11 +271,11 @@ template <typename Kernel>
 cudaError_t persistent_grid(Kernel kernel, int threads, int smem, int ctas_per_sm,
                             int64_t rows, const DeviceInfo* dev, int* grid) {
   int resident = 0;
-  cudaError_t e = resident_ctas(kernel, threads, smem, &resident);
+  cudaError_t e = resident_ctas(kernel, threads, smem, dev->id, &resident);
   if (e != cudaSuccess) return e;
   if (resident < 1) return cudaErrorInvalidConfiguration;
   const int per_sm = ctas_per_sm < resident ? ctas_per_sm : resident;
-  int64_t g = static_cast<int64_t>(dev->sms) * per_sm;
+  int64_t g = static_cast<int64_t>(dev->sms.load(std::memory_order_relaxed)) * per_sm;
   if (g > rows) g = rows;
   *grid = static_cast<int>(g);
   return cudaSuccess;
