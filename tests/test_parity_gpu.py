@@ -516,3 +516,53 @@ def test_dynamic_schedule_chained_with_other_kernels_on_one_stream():
                        outs["out_scales"].cpu().numpy()))
     for a, b in zip(finals[0], finals[1]):
         assert np.array_equal(a, b)
+
+
+# ------------------------------------------------------------------------- exact ties
+def _tie_inputs(weights: list[float], rows: int = 8, mode: str = "none", scale=None) -> dict:
+    """tp = 1, no residual, no bias, every h = +-1 (so mean(h^2) = 1) and eps = 1e-30 (so
+    mean + eps rounds to exactly 1 in fp32): y = h * w exactly when the kernel's rsqrt(1) is 1."""
+    H = len(weights)
+    g = torch.Generator(device="cpu").manual_seed(11)
+    signs = (torch.randint(0, 2, (1, rows, H), generator=g) * 2 - 1).to(torch.bfloat16)
+    return dict(partials=signs.to(DEV), residual=None, addend=None, bias=None,
+                weight=torch.tensor(weights, dtype=torch.bfloat16, device=DEV),
+                tp=1, T_pad=rows, T_valid=rows, H=H, eps=1e-30, mode=mode, scale=scale)
+
+
+def _rsqrt_of_one_is_exact() -> bool:
+    inp = _tie_inputs([1.0] * 16)
+    out = run_gpu(inp)["out"].view(np.uint16)
+    return bool(np.all((out == 0x3F80) | (out == 0xBF80)))  # +-1.0 in bf16
+
+
+def test_fp8_codes_round_exact_ties_to_even():
+    """E4M3 midpoints (values with one more mantissa bit than E4M3 holds) as quantiser inputs:
+    the kernel's codes equal the oracle's ties-to-even codes bit for bit."""
+    if not _rsqrt_of_one_is_exact():
+        pytest.skip("rsqrt(1) is not exactly 1 on this device: no exact ties to feed")
+    mids = []
+    for e in (-6, -3, 0, 2, 7):              # normal binades of E4M3 (2^-6 .. 2^8)
+        for k in range(8):                   # mantissa m/8, midpoint (2k+1)/16 above 1
+            mids.append((1.0 + (2 * k + 1) / 16.0) * 2.0 ** e)
+    mids += [-m for m in mids[:24]]
+    mids += [0.5 * 2.0 ** -9, 1.5 * 2.0 ** -9, 2.5 * 2.0 ** -9]   # subnormal midpoints
+    while len(mids) % 16:
+        mids.append(1.0)
+    inp = _tie_inputs(mids, mode="fp8_static", scale=1.0)
+    got = run_gpu(inp)["out"]
+    ref = run_oracle(inp)["out"]
+    assert np.array_equal(got, ref)
+
+
+def test_nvfp4_codes_round_exact_ties_to_even():
+    """E2M1 midpoints in 16-element blocks whose largest magnitude is 6 (so with a global scale
+    of 1 every block scale is exactly 1): codes equal the oracle's ties-to-even codes."""
+    if not _rsqrt_of_one_is_exact():
+        pytest.skip("rsqrt(1) is not exactly 1 on this device: no exact ties to feed")
+    block = [6.0, 0.25, 0.75, 1.25, 1.75, 2.5, 3.5, 5.0, -0.25, -0.75, -1.25, -1.75, -2.5, -3.5,
+             -5.0, 1.0]
+    inp = _tie_inputs(block * 4, mode="nvfp4", scale=1.0)
+    got, ref = run_gpu(inp), run_oracle(inp)
+    assert np.array_equal(got["out_scales"], ref["out_scales"])
+    assert np.array_equal(got["out"], ref["out"])
