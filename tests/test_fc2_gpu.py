@@ -50,3 +50,45 @@ def test_fc2_reorganize_matches_oracle(G, P, N, H, dtype):
                                 else x.cpu().numpy(), P)
     got = outs[0].view(torch.uint8).numpy().reshape(ref.shape[0], ref.shape[1], -1)
     assert np.array_equal(got, ref.view(np.uint8).reshape(got.shape))
+
+
+def test_fc2_reads_what_the_fused_stage_just_wrote():
+    """Fused stage then reorganisation on one stream, both launched with programmatic dependent
+    launch: the reorganisation reads the new residual the fused call has just written (it must
+    wait for that grid), in a loop and replayed from a CUDA graph."""
+    from sequence_reduce_add_gb300 import synth
+    w = synth.workload(2)
+    inp = synth.make_inputs(w, device=DEV, T_pad=1024, T_valid=1024)
+    G, P, F = 8, 2, 512
+    N = 1024 * 4096 // (G * F)
+    D = G // P
+    res_out = torch.empty((1024, 4096), dtype=torch.bfloat16, device=DEV)
+    out = torch.empty_like(res_out)
+    y = torch.empty((G, N // D, D * F), dtype=torch.bfloat16, device=DEV)
+    s = torch.cuda.Stream(device=DEV)
+
+    def step():
+        sp.sp_fused_reduce_norm(inp["partials"], inp["weight"], out, res_out,
+                                residual=inp["residual"], bias=inp["bias"], stream=s)
+        sp.sp_fc2_reorganize(res_out.view(G, N, F), P, y, stream=s)
+
+    def check():
+        torch.cuda.synchronize()
+        x = res_out.view(torch.int16).cpu().numpy().view(np.uint16).reshape(G, N, F)
+        ref = oracle.fc2_reorganize(x, P)
+        assert np.array_equal(y.view(torch.int16).cpu().numpy().view(np.uint16), ref)
+
+    for k in range(5):
+        inp["partials"].mul_(0.5 if k % 2 else 2.0)   # new contents every step
+        step()
+        check()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g, stream=s):
+        step()
+    inp["residual"].mul_(-1.0)
+    torch.cuda.synchronize()
+    g.replay()
+    check()
