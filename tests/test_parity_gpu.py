@@ -566,3 +566,33 @@ def test_nvfp4_codes_round_exact_ties_to_even():
     got, ref = run_gpu(inp), run_oracle(inp)
     assert np.array_equal(got["out_scales"], ref["out_scales"])
     assert np.array_equal(got["out"], ref["out"])
+
+
+def test_dynamic_schedule_soak_two_chained_streams():
+    """100 calls in place on each of two streams at once, back to back (consecutive calls
+    overlap through programmatic dependent launch): every call reads the residual the previous
+    one wrote, so a row skipped or done twice anywhere would change the end result. Dynamic and
+    static schedules must end byte-identical."""
+    w = synth.workload(3)
+    streams = [torch.cuda.Stream(device=DEV) for _ in range(2)]
+    inps = [synth.make_inputs(w, device=DEV, T_pad=4096, T_valid=4093, H=7168, seed=77 + k)
+            for k in range(2)]
+    scale = torch.tensor([w["scale"]], device=DEV)
+    ends = []
+    for schedule in ("dynamic", "static"):
+        res = [i["residual"].clone() for i in inps]
+        outs = [sp.allocate_outputs(4096, 7168, w["mode"], DEV) for _ in inps]
+        torch.cuda.synchronize()
+        for _ in range(100):
+            for k, s in enumerate(streams):
+                i = inps[k]
+                sp.sp_fused_reduce_norm_ex(sp.sp_options_init(schedule=schedule), i["partials"],
+                                           i["weight"], outs[k]["out"], res[k], residual=res[k],
+                                           bias=i["bias"], eps=i["eps"], quant_mode=i["mode"],
+                                           scale=scale, T_valid=i["T_valid"], stream=s)
+        torch.cuda.synchronize()
+        ends.append([(r.view(torch.int16).cpu().numpy(), o["out"].cpu().numpy())
+                     for r, o in zip(res, outs)])
+    for (ra, oa), (rb, ob) in zip(ends[0], ends[1]):
+        assert np.array_equal(ra, rb) and np.array_equal(oa, ob)
+    assert sp.sp_device_error(clear=False) == 0
