@@ -151,7 +151,7 @@ sp_status sp_check_args(const void* partials, int tp, int64_t T_pad, int64_t T_v
  *                  counter of the call's stream, so CTAs that get more memory bandwidth take more
  *                  rows (applies to the staged kernel, the one device-buffer calls use).
  *                  SP_SCHEDULE_AUTO (the default): dynamic when the staged kernel gives every CTA
- *                  at least 10 rows and H >= 2048, static otherwise.
+ *                  at least 10 rows, H >= 2048 and (tp + 3) * 2H >= 24 KB, static otherwise.
  *                  The counters are a fixed table in the library's device memory (no allocation):
  *                  one slot per stream (told apart by cudaStreamGetId), reset by each call's last
  *                  CTA, so calls on one stream reuse it in stream order and calls on different

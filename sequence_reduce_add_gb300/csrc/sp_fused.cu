@@ -153,12 +153,14 @@ sp_status device_info(DeviceInfo** info) {
 
 int vec_index(int vec) { return vec == 1 ? 0 : vec == 2 ? 1 : 2; }
 
-// The dynamic schedule pays off once every CTA has this many rows (measured on GB300: 1-5 %
-// faster from about 11 rows per CTA, 1.5 % slower at 7) and rows are at least this wide: at
-// H = 1024 (16 CTAs per SM, 14 KB per row at tp = 4) the claims on one counter come too fast and
-// it was 29 % slower (4.5 vs 6.3 TB/s at T = 32768); from H = 2048 it is 1-2 % faster.
+// The dynamic schedule pays off once every CTA has this many rows (measured on GB300: 1-13 %
+// faster from about 11 rows per CTA, 1.5 % slower at 7) and each row moves enough bytes that the
+// claims on the one counter stay rare: with (tp + 3) * 2H bytes per row (partials, residual,
+// residual_out, bf16 out) below ~24 KB it lost (tp=4, H=1024, 14 KB: 29 % slower, 4.5 vs 6.3
+// TB/s at T = 32768; tp=2, H=2048, 20 KB: 1.7 % slower); from 28 KB up it won.
 constexpr int64_t kDynamicMinRowsPerCta = 10;
 constexpr int64_t kDynamicMinHidden = 2048;
+constexpr int64_t kDynamicMinRowBytes = 24 * 1024;
 
 // Row counter slot of `stream` on this device, or -1: the call then uses the static schedule.
 // No slot while the stream is being captured (a replay of the graph may run beside later calls
@@ -331,7 +333,8 @@ cudaError_t launch_one(const sp_launch_config& cfg, spk::Params& p, int smem, in
   const bool want_dynamic =
       schedule == SP_SCHEDULE_DYNAMIC ||
       (schedule == SP_SCHEDULE_AUTO && p.rows_total >= kDynamicMinRowsPerCta * grid &&
-       p.H >= kDynamicMinHidden);
+       p.H >= kDynamicMinHidden &&
+       static_cast<int64_t>(p.tp + 3) * 2 * p.H >= kDynamicMinRowBytes);
   if (want_dynamic && p.rows_total + grid < (int64_t{1} << 31)) slot = counter_slot(dev, stream);
   if (slot >= 0) {
     // The dynamic variant's own occupancy sizes its grid: every CTA must be resident from the
