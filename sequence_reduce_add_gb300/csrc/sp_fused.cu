@@ -111,6 +111,8 @@ sp_status check(const void* partials, int tp, int64_t T_pad, int64_t T_valid, in
 
 // ------------------------------------------------------------------------------ devices
 constexpr int kMaxDevices = 64;
+// GB300's SM count, for launch choices made without querying a device.
+constexpr int64_t kSmsHint = 152;
 constexpr int kSmemPerSm = 233472;   // 228 KiB of shared memory per SM
 constexpr int kSmemPerCtaMax = 232448;  // 227 KiB opt-in limit per CTA
 // FlashComm2 reorganisation: bulk-copy tiles of at most this many bytes, ring stages per CTA,
@@ -488,7 +490,10 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   //                        2 KB segments leave the ring little to hide: 10-35 % faster);
   //   4096 < H <= 8192:    direct while tp * T * H <= 2^20 (13-30 % faster at T = 8-64);
   //                        for 64-128 rows, the staged kernel at one CTA per SM with every
-  //                        stage that fits (a 12-stage ring at H = 8192: 10-34 % faster).
+  //                        stage that fits (a 12-stage ring at H = 8192: 10-34 % faster);
+  //   4096 < H <= 6144, more rows than SMs but no more than one round of the large-call grid:
+  //                        ceil(T / SMs) CTAs per SM, every stage that fits (6-27 % faster at
+  //                        T = 160-456; at H = 4096 and from 7168 up it was a wash).
   const int64_t elems = static_cast<int64_t>(tp) * T_pad * H;
   bool direct = false;
   bool deep_ring = false;
@@ -515,6 +520,15 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   } else if (deep_ring_1 && c.kernel == SP_KERNEL_STAGED && max_stages(H, 1) >= c.stages) {
     c.ctas_per_sm = 1;
     c.stages = 0;
+  } else if (!direct && c.kernel == SP_KERNEL_STAGED && H > 4096 && H <= 6144 &&
+             T_pad > kSmsHint && T_pad <= kSmsHint * c.ctas_per_sm) {
+    // All rows fit in one round of the large-call grid: each CTA has at most one row, so use
+    // only as many CTAs per SM as the rows need and give each the deepest ring that fits.
+    const int want = static_cast<int>((T_pad + kSmsHint - 1) / kSmsHint);
+    if (max_stages(H, want) >= c.stages) {
+      c.ctas_per_sm = want;
+      c.stages = 0;
+    }
   }
   *config = c;
   return SP_OK;
