@@ -114,10 +114,10 @@ def test_launch_selection(lib):
     (16, 256, 7168, (0, 2, 2, 4)),
     (8, 256, 5120, (0, 2, 2, 0)),       # one round of rows at H = 5120: 2 CTAs/SM, deep ring
     (8, 384, 5120, (0, 2, 3, 0)),
-    (8, 512, 5120, (0, 2, 3, 3)),       # more than one round: the large-call launch
+    (8, 512, 5120, (0, 2, 3, 4)),       # more than one round: the large-call launch
     (4, 4096, 4096, (0, 2, 4, 3)),      # large: staged, CTAs/SM = 16384 / H
     (8, 8192, 7168, (0, 2, 2, 4)),
-    (8, 16384, 5120, (0, 2, 3, 3)),
+    (8, 16384, 5120, (0, 2, 3, 4)),
 ])
 def test_launch_rule(lib, tp, T, H, want):
     c = sp.sp_select_launch(tp, T, H, "none")
