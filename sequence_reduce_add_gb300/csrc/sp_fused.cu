@@ -494,7 +494,10 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   //                        stage that fits (a 12-stage ring at H = 8192: 10-34 % faster);
   //   4096 < H <= 6144, more rows than SMs but no more than one round of the large-call grid:
   //                        ceil(T / SMs) CTAs per SM, every stage that fits (6-27 % faster at
-  //                        T = 160-456; at H = 4096 and from 7168 up it was a wash).
+  //                        T = 160-456; at H = 4096 and from 7168 up it was a wash);
+  //   H >= 4096, between one and two rounds of the large-call grid: the CTAs per SM whose last
+  //                        round is fullest, every stage that fits (5-21 % faster at H = 4096
+  //                        and 5120, T = 512-896).
   const int64_t elems = static_cast<int64_t>(tp) * T_pad * H;
   bool direct = false;
   bool deep_ring = false;
@@ -528,6 +531,24 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     const int want = static_cast<int>((T_pad + kSmsHint - 1) / kSmsHint);
     if (max_stages(H, want) >= c.stages) {
       c.ctas_per_sm = want;
+      c.stages = 0;
+    }
+  } else if (!direct && c.kernel == SP_KERNEL_STAGED && H >= 4096 &&
+             T_pad > kSmsHint * c.ctas_per_sm && T_pad < 2 * kSmsHint * c.ctas_per_sm) {
+    // Between one and two rounds of rows: the second round runs part-empty. Take the CTAs per
+    // SM (at most the large-call count, at least 2, and no fewer than leave each CTA 3 rows)
+    // whose last round is fullest, ties to more CTAs, with the deepest ring that fits. With more
+    // rows per CTA the SMs' bandwidth needs several CTAs each (1 CTA/SM at 6.7 rows: 50 % slower);
+    // one CTA per SM was mixed even at 2-3 rows (-13 % to +13 %).
+    auto rounds = [&](int ctas) {
+      return static_cast<double>(T_pad) / static_cast<double>(kSmsHint * ctas);
+    };
+    auto fill = [&](int ctas) { return rounds(ctas) / std::ceil(rounds(ctas)); };
+    int best = c.ctas_per_sm;
+    for (int ctas = c.ctas_per_sm - 1; ctas >= 2 && rounds(ctas) <= 3.0; --ctas)
+      if (fill(ctas) > fill(best) + 1e-9) best = ctas;
+    if (best != c.ctas_per_sm && max_stages(H, best) >= c.stages) {
+      c.ctas_per_sm = best;
       c.stages = 0;
     }
   }
