@@ -596,3 +596,23 @@ def test_dynamic_schedule_soak_two_chained_streams():
     for (ra, oa), (rb, ob) in zip(ends[0], ends[1]):
         assert np.array_equal(ra, rb) and np.array_equal(oa, ob)
     assert sp.sp_device_error(clear=False) == 0
+
+
+# ------------------------------------------------------------------------- launch-rule bands
+@pytest.mark.parametrize("tp,T,H,mode,band", [
+    (4, 32, 8192, "fp8_per_token", (1, 2, 8, 0)),     # direct, two vectors per thread
+    (16, 64, 4096, "none", (0, 2, 2, 0)),             # staged, deep ring at 2 CTAs/SM
+    (8, 96, 7168, "nvfp4", (0, 2, 1, 0)),             # staged, one CTA per SM
+    (8, 256, 5120, "fp8_static", (0, 2, 2, 0)),       # one round of rows, fewest CTAs
+    (4, 768, 4096, "none", (0, 2, 3, 0)),             # last round filled at 3 CTAs/SM
+    (8, 512, 5120, "fp8_per_token", (0, 2, 2, 0)),    # last round filled at 2 CTAs/SM
+    (4, 4096, 1024, "none", (1, 1, 16, 0)),           # direct up to 2^22 elements at H = 1024
+    (8, 1536, 4096, "nvfp4", (0, 2, 4, 3)),           # the large-call launch
+])
+def test_default_launch_in_each_band(tp, T, H, mode, band):
+    """Each band of the launch rule, checked to be the band and compared with the oracle."""
+    c = sp.sp_select_launch(tp, T, H, mode)
+    assert (c.kernel, c.vec_per_thread, c.ctas_per_sm, c.stages) == band
+    w = dict(synth.workload(3), mode=mode, scale=0.05 if mode == "fp8_static" else None)
+    inp = synth.make_inputs(w, device=DEV, tp=tp, T_pad=T, T_valid=T - 3, H=H)
+    assert _check(inp)
