@@ -539,13 +539,15 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     // SM (at most the large-call count, at least 2, and no fewer than leave each CTA 3 rows)
     // whose last round is fullest, ties to more CTAs, with the deepest ring that fits. With more
     // rows per CTA the SMs' bandwidth needs several CTAs each (1 CTA/SM at 6.7 rows: 50 % slower);
-    // one CTA per SM was mixed even at 2-3 rows (-13 % to +13 %).
+    // one CTA per SM at 2-3 rows paid only for long rows (H >= 7168, tp >= 8: up to 13 % faster;
+    // tp = 4 or H = 6144: -13 % to +4 %).
     auto rounds = [&](int ctas) {
       return static_cast<double>(T_pad) / static_cast<double>(kSmsHint * ctas);
     };
     auto fill = [&](int ctas) { return rounds(ctas) / std::ceil(rounds(ctas)); };
     int best = c.ctas_per_sm;
-    for (int ctas = c.ctas_per_sm - 1; ctas >= 2 && rounds(ctas) <= 3.0; --ctas)
+    const int fewest = (H >= 7168 && tp >= 8) ? 1 : 2;
+    for (int ctas = c.ctas_per_sm - 1; ctas >= fewest && rounds(ctas) <= 3.0; --ctas)
       if (fill(ctas) > fill(best) + 1e-9) best = ctas;
     if (best != c.ctas_per_sm && max_stages(H, best) >= c.stages) {
       c.ctas_per_sm = best;

@@ -117,7 +117,8 @@ def test_launch_selection(lib):
     (8, 512, 5120, (0, 2, 2, 0)),       # 1.1 rounds at 3 CTAs/SM: 2 CTAs/SM fill the last one
     (4, 768, 4096, (0, 2, 3, 0)),       # 1.3 rounds at 4 CTAs/SM: 3 fill it better
     (4, 1024, 4096, (0, 2, 4, 3)),      # fewer CTAs would leave each more than 3 rows
-    (8, 384, 7168, (0, 2, 2, 4)),       # 1.3 rounds at 2 CTAs/SM, but never below 2 CTAs/SM
+    (8, 384, 7168, (0, 2, 1, 0)),       # 1.3 rounds at 2 CTAs/SM; long rows: one CTA per SM
+    (4, 384, 7168, (0, 2, 2, 4)),       # ... but not at tp = 4
     (4, 4096, 4096, (0, 2, 4, 3)),      # large: staged, CTAs/SM = 16384 / H
     (8, 8192, 7168, (0, 2, 2, 4)),
     (8, 16384, 5120, (0, 2, 3, 4)),
