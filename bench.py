@@ -165,6 +165,10 @@ VARIANTS = {
     "swizzled_scales": dict(scale_layout=1),
 }
 # (workload, variant) pairs measured beside the other workloads
+# Decode-sized calls (tp, tokens, H) of the per-token FP8 workload's kind: latency-bound, so each
+# is also timed replayed from a CUDA graph.
+DECODE_RUNS = [(8, 8, 8192), (8, 64, 8192), (8, 256, 8192)]
+
 VARIANT_RUNS = [("tp4_T4093p4096_H4096_bf16", "first"),
                 ("tp4_T4093p4096_H4096_bf16", "scaled_addend"),
                 ("tp8_T16384_H5120_nvfp4", "swizzled_scales")]
@@ -446,6 +450,11 @@ def run_ours(args) -> None:
         for name, variant in VARIANT_RUNS:
             extras[f"{name}+{variant}"] = bench_extra(lib, sp, synth, synth.workload(name),
                                                       device, stream, peak, variant)
+        for tp, T, H in DECODE_RUNS:
+            dw = dict(synth.workload("tp16_T3500p3504_H8192_fp8pertoken"), tp=tp, T_valid=T,
+                      T_pad=T, H=H, name=f"decode_tp{tp}_T{T}_H{H}_fp8pertoken")
+            extras[dw["name"]] = bench_extra(lib, sp, synth, dw, device, stream, peak,
+                                             seed=synth.BASE_SEED + 100 + T)
         extras["fc2_reorganize_G8_otp2_N8192_H7168_bf16"] = bench_fc2(lib, device, stream, peak)
 
     if rank != 0:
@@ -489,9 +498,12 @@ def run_ours(args) -> None:
     print(json.dumps(line), flush=True)
 
 
-def bench_extra(lib, sp, synth, w, device, stream, peak, variant: str | None = None) -> dict:
+def bench_extra(lib, sp, synth, w, device, stream, peak, variant: str | None = None,
+                seed: int | None = None) -> dict:
     """Per-workload kernel figures for the other workloads (rotating sets, CUDA events)."""
-    base = Problem(w, synth.BASE_SEED + 1 + synth.WORKLOADS.index(w), device, sp, variant)
+    if seed is None:
+        seed = synth.BASE_SEED + 1 + synth.WORKLOADS.index(w)
+    base = Problem(w, seed, device, sp, variant)
     sets = max(2, min(6, -(-(4 * L2_BYTES) // base.nbytes())))
     problems = [base] + [Problem(w, base.inp["seed"] + 1000 * k, device, sp, variant)
                          for k in range(1, sets)]
