@@ -159,9 +159,15 @@ sp_status sp_check_args(const void* partials, int tp, int64_t T_pad, int64_t T_v
  *                  stream is being captured into a CUDA graph (a replay may run beside calls on
  *                  the capturing stream) and when all slots are taken. Any other value is
  *                  SP_ERR_UNSUPPORTED.
+ *   launch         a launch configuration (below) to run instead of the one sp_select_launch
+ *                  picks, for tests and tuning; NULL (the default) = the library's choice. The
+ *                  checks of sp_fused_reduce_norm_with_config apply. With host_buffers = 1 it
+ *                  must name the DIRECT kernel (else SP_ERR_UNSUPPORTED).
  */
 enum { SP_SCALES_ROW_MAJOR = 0, SP_SCALES_SWIZZLED_128X4 = 1 };
 enum { SP_SCHEDULE_AUTO = 0, SP_SCHEDULE_STATIC = 1, SP_SCHEDULE_DYNAMIC = 2 };
+
+struct sp_launch_config;
 
 typedef struct sp_fused_options {
   float partial_scale;
@@ -169,6 +175,7 @@ typedef struct sp_fused_options {
   int scale_layout;
   int host_buffers;
   int schedule;
+  const struct sp_launch_config* launch;
 } sp_fused_options;
 
 void sp_options_init(sp_fused_options* options /* host, out */);
@@ -222,6 +229,13 @@ sp_status sp_fused_reduce_norm_host(const void* partials, int tp, int64_t T_pad,
  *                   this kernel an SM can hold), capped at T_pad; 1 .. 32.
  *   stages          shared-memory ring depth in row segments of 2*H bytes (STAGED only); 0 picks
  *                   the deepest ring that fits ctas_per_sm CTAs on an SM.
+ *   split           CTAs that share each row (DIRECT only, vec_per_thread 1 or 2): 0 or 1, a row
+ *                   per CTA; 2, 4 or 8, a thread-block cluster of that many CTAs per row, each
+ *                   owning a contiguous slice of it and combining the row's sum of squares (and
+ *                   max) through distributed shared memory, so that a call with few rows uses
+ *                   `split` times as many SMs. Grid = split x min(T rows, SMs x ctas_per_sm /
+ *                   split) CTAs. Another value is SP_ERR_INVALID_ARG; split > 1 with the STAGED
+ *                   kernel or vec_per_thread 4 is SP_ERR_UNSUPPORTED.
  */
 enum { SP_KERNEL_STAGED = 0, SP_KERNEL_DIRECT = 1 };
 
@@ -230,6 +244,7 @@ typedef struct sp_launch_config {
   int vec_per_thread;
   int ctas_per_sm;
   int stages;
+  int split;
 } sp_launch_config;
 
 sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,

@@ -45,24 +45,25 @@ class SpError(RuntimeError):
         super().__init__(f"{where}: {STATUS_NAMES.get(status, status)}")
 
 
-class Options(ctypes.Structure):
-    """sp_fused_options: partial_scale, addend (device address or None), scale_layout,
-    host_buffers, schedule."""
-    _fields_ = [("partial_scale", ctypes.c_float), ("addend", ctypes.c_void_p),
-                ("scale_layout", ctypes.c_int), ("host_buffers", ctypes.c_int),
-                ("schedule", ctypes.c_int)]
-
-
-SCHEDULES = {"auto": 0, "static": 1, "dynamic": 2}
-
-
 class LaunchConfig(ctypes.Structure):
-    """sp_launch_config: kernel (0 staged, 1 direct), vec_per_thread, ctas_per_sm, stages."""
+    """sp_launch_config: kernel (0 staged, 1 direct), vec_per_thread, ctas_per_sm, stages,
+    split (CTAs of a cluster per row; 0 or 1 = one CTA per row)."""
     _fields_ = [("kernel", ctypes.c_int), ("vec_per_thread", ctypes.c_int),
-                ("ctas_per_sm", ctypes.c_int), ("stages", ctypes.c_int)]
+                ("ctas_per_sm", ctypes.c_int), ("stages", ctypes.c_int), ("split", ctypes.c_int)]
 
     def as_dict(self) -> dict:
         return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class Options(ctypes.Structure):
+    """sp_fused_options: partial_scale, addend (device address or None), scale_layout,
+    host_buffers, schedule, launch (a LaunchConfig or None)."""
+    _fields_ = [("partial_scale", ctypes.c_float), ("addend", ctypes.c_void_p),
+                ("scale_layout", ctypes.c_int), ("host_buffers", ctypes.c_int),
+                ("schedule", ctypes.c_int), ("launch", ctypes.POINTER(LaunchConfig))]
+
+
+SCHEDULES = {"auto": 0, "static": 1, "dynamic": 2}
 
 
 _MAIN_ARGS = [_vp, ctypes.c_int, _i64, _i64, _i64, _vp, _vp, _vp, ctypes.c_float, ctypes.c_int,
@@ -176,9 +177,10 @@ def sp_fused_reduce_norm(partials, weight, out, residual_out, *, residual=None, 
 
 
 def sp_options_init(*, partial_scale: float = 1.0, addend=None, scale_layout: int = 0,
-                    host_buffers: bool = False, schedule="auto") -> Options:
+                    host_buffers: bool = False, schedule="auto", launch=None) -> Options:
     """An sp_fused_options initialised by the library, then set from the keywords (``addend`` is a
-    tensor or None; ``schedule`` is "auto", "static", "dynamic" or the enum value)."""
+    tensor or None; ``schedule`` is "auto", "static", "dynamic" or the enum value; ``launch`` a
+    LaunchConfig, a dict of its fields, or None for the library's choice)."""
     o = Options()
     load_library().sp_options_init(ctypes.byref(o))
     o.partial_scale = partial_scale
@@ -186,6 +188,10 @@ def sp_options_init(*, partial_scale: float = 1.0, addend=None, scale_layout: in
     o.scale_layout = scale_layout
     o.host_buffers = 1 if host_buffers else 0
     o.schedule = SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
+    if launch is not None:
+        cfg = LaunchConfig(**launch) if isinstance(launch, dict) else launch
+        o._launch_ref = cfg  # the struct must outlive the options that point at it
+        o.launch = ctypes.pointer(cfg)
     return o
 
 

@@ -47,6 +47,7 @@ struct Params {
   int wb_offset;              // staged kernel: byte offset of the weight/bias copy [2][H] bf16
   int ring_offset;            // staged kernel: byte offset of the ring in dynamic shared memory
   int counter_slot;           // dynamic schedule: row counter slot of the launch's stream
+  int split_chunk;            // split rows: 16-byte vectors of a row per CTA of the cluster
 };
 
 // Per-warp slot of the row reduction: sum of squares, max |h*w| and an abort vote.
@@ -326,6 +327,44 @@ __device__ __forceinline__ void named_barrier_sync(int id, int nthreads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
 }
 
+// ---------------------------------------------------------------- thread-block clusters
+__device__ __forceinline__ int cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return static_cast<int>(r);
+}
+// Every thread of every CTA of the cluster: writes before it are seen by reads after it.
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+               ::: "memory");
+}
+// Two floats from CTA `rank`'s copy of this CTA's shared-memory address `addr`.
+__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t addr, int rank) {
+  uint32_t remote;
+  float2 v;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
+  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(remote)
+               : "memory");
+  return v;
+}
+// Split rows: the CTA-wide (sum of squares, max) of each CTA of the cluster, combined in rank
+// order (the same sum in every CTA). cslots: two slots in this CTA's shared memory, used on
+// alternate rows, so one cluster barrier per row suffices.
+template <int kSplit>
+__device__ __forceinline__ float2 cluster_row_sum(float2 part, float2* cslots, int parity) {
+  if (threadIdx.x == 0) cslots[parity] = part;
+  cluster_sync();
+  const uint32_t addr = smem_addr(cslots + parity);
+  float ss = 0.0f, mx = 0.0f;
+#pragma unroll
+  for (int r = 0; r < kSplit; ++r) {
+    const float2 v = ld_cluster_f32x2(addr, r);
+    ss += v.x;
+    mx = fmaxf(mx, v.y);
+  }
+  return make_float2(ss, mx);
+}
+
 // ---------------------------------------------------------------- row reduction
 // Sum of squares and (optionally) max over the CTA's consumer threads, plus an OR of their abort
 // votes. All consumer threads get bit-identical results (every thread adds the per-warp values
@@ -399,18 +438,29 @@ __device__ __forceinline__ bool is_scale_pad_vector(const Params& p, int v) {
   return p.scale_swizzled && v >= p.nvec && (v & 1) == 0 && v < 2 * p.sf_cols;
 }
 
+// Split rows: the swizzled layout's padding scale columns of row t, written by thread 0 of the
+// cluster's first CTA.
+__device__ __forceinline__ void zero_scale_pad_columns(const Params& p, int64_t t, int c,
+                                                       int vbase) {
+  if (!p.scale_swizzled || c != 0 || vbase != 0) return;
+  uint8_t* sf_row = static_cast<uint8_t*>(p.out_scales) + scale_row_base(p, t);
+  for (int b = p.H / 16; b < p.sf_cols; ++b) sf_row[scale_col_offset(p, b)] = 0;
+}
+
 // Zero every output byte of padding row t that this thread owns. Rows at or beyond T_pad exist
 // only in the swizzled NVFP4 scale layout (rows padded to 128): there only the scales are written.
-template <int kVec, int kMode>
-__device__ __forceinline__ void zero_row(const Params& p, int64_t t, int c) {
+// Split rows (kSplit > 1): this CTA owns vectors [vbase, vend) of the row.
+template <int kVec, int kMode, int kSplit = 1>
+__device__ __forceinline__ void zero_row(const Params& p, int64_t t, int c, int vbase = 0,
+                                         int vend = 0) {
   const int64_t H = p.H;
   const bool real_row = t < p.T_pad;
 #pragma unroll
   for (int k = 0; k < kVec; ++k) {
-    const int v = c + k * p.nthreads;
-    if (kMode == kModeNvfp4 && is_scale_pad_vector(p, v))
+    const int v = (kSplit > 1 ? vbase : 0) + c + k * p.nthreads;
+    if (kMode == kModeNvfp4 && kSplit == 1 && is_scale_pad_vector(p, v))
       static_cast<uint8_t*>(p.out_scales)[scale_offset(p, t, v / 2)] = 0;
-    if (v >= p.nvec) continue;
+    if (v >= (kSplit > 1 ? vend : p.nvec)) continue;
     if (real_row) stg_stream(p.residual_out + t * H + v * 8, make_uint4(0, 0, 0, 0));
     if (kMode != kModeNvfp4 && !real_row) continue;
     if (kMode == kModeNone) {
@@ -422,22 +472,29 @@ __device__ __forceinline__ void zero_row(const Params& p, int64_t t, int c) {
       if ((v & 1) == 0) static_cast<uint8_t*>(p.out_scales)[scale_offset(p, t, v / 2)] = 0;
     }
   }
-  if (kMode == kModeFp8PerToken && c == 0 && real_row) static_cast<float*>(p.out_scales)[t] = 0.0f;
+  if (kMode == kModeFp8PerToken && c == 0 && (kSplit == 1 || vbase == 0) && real_row)
+    static_cast<float*>(p.out_scales)[t] = 0.0f;
+  if (kMode == kModeNvfp4 && kSplit > 1) zero_scale_pad_columns(p, t, c, vbase);
 }
 
 // Finish row t: h holds sum_r partials + residual + bias for this thread's vectors (zero for
 // vectors past the row). Writes residual_out, normalises, quantises and stores. Returns the
-// CTA-wide abort vote.
-template <int kVec, int kMode>
+// CTA-wide abort vote. Split rows (kSplit > 1): this CTA owns vectors [vbase, vend) and the row's
+// sums are combined across the cluster through cslots.
+template <int kVec, int kMode, int kSplit = 1>
 __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)[kVec][8],
                                           const uint4 (&w)[kVec], const QuantConst& qc,
-                                          RedSlot* slots, int parity, int c, int abort) {
+                                          RedSlot* slots, int parity, int c, int abort,
+                                          int vbase = 0, int vend = 0,
+                                          float2* cslots = nullptr) {
   const int64_t H = p.H;
+  const int v0 = kSplit > 1 ? vbase : 0;
+  const int vlim = kSplit > 1 ? vend : p.nvec;
   float ss0 = 0.0f, ss1 = 0.0f;  // sums of squares of the even and the odd elements
 #pragma unroll
   for (int k = 0; k < kVec; ++k) {
-    const int v = c + k * p.nthreads;
-    if (v < p.nvec) stg_stream(p.residual_out + t * H + v * 8, pack_bf16x8(h[k]));
+    const int v = v0 + c + k * p.nthreads;
+    if (v < vlim) stg_stream(p.residual_out + t * H + v * 8, pack_bf16x8(h[k]));
 #pragma unroll
     for (int e = 0; e < 8; e += 2) fma2(ss0, ss1, h[k][e], h[k][e + 1], h[k][e], h[k][e + 1]);
   }
@@ -455,25 +512,26 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
     }
   }
   int abort_all = 0;
-  const float2 red =
+  float2 red =
       row_reduce<kMode == kModeFp8PerToken>(ss, mx, abort, slots, parity, p.nthreads, &abort_all);
+  if constexpr (kSplit > 1) red = cluster_row_sum<kSplit>(red, cslots, parity);
   const float rinv = rsqrtf(red.x / static_cast<float>(p.H) + p.eps);
 
   if (kMode == kModeNone) {
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
-      const int v = c + k * p.nthreads;
+      const int v = v0 + c + k * p.nthreads;
       scale8(h[k], rinv);
-      if (v < p.nvec) stg_stream(static_cast<uint16_t*>(p.out) + t * H + v * 8, pack_bf16x8(h[k]));
+      if (v < vlim) stg_stream(static_cast<uint16_t*>(p.out) + t * H + v * 8, pack_bf16x8(h[k]));
     }
   } else if (kMode == kModeFp8Static) {
     const float rinv_q = rinv * qc.inv_scale;  // y / scale = h*w * (rinv / scale)
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
-      const int v = c + k * p.nthreads;
+      const int v = v0 + c + k * p.nthreads;
       float* q = h[k];
       scale8(h[k], rinv_q);
-      if (v < p.nvec)
+      if (v < vlim)
         stg_stream(static_cast<uint8_t*>(p.out) + t * H + v * 8,
                    make_uint2(pack_e4m3x4(q[0], q[1], q[2], q[3]),
                               pack_e4m3x4(q[4], q[5], q[6], q[7])));
@@ -482,18 +540,18 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
     // s_t = max|y| / 448 with max|y| = max|h*w| * rinv; the codes are y / s_t = h*w * 448/max|h*w|
     const float mxhw = red.y;
     const float s = (mxhw * rinv) / 448.0f;
-    if (c == 0) static_cast<float*>(p.out_scales)[t] = s;
+    if (c == 0 && v0 == 0) static_cast<float*>(p.out_scales)[t] = s;
     float f = 448.0f / mxhw;
     const bool by_division = !(f <= 3.0e38f);  // max|h*w| is zero or tiny
     if (s == 0.0f) f = 0.0f;
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
-      const int v = c + k * p.nthreads;
+      const int v = v0 + c + k * p.nthreads;
       float q[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e)
         q[e] = (by_division && s != 0.0f) ? __fdiv_rn(h[k][e], mxhw) * 448.0f : h[k][e] * f;
-      if (v < p.nvec)
+      if (v < vlim)
         stg_stream(static_cast<uint8_t*>(p.out) + t * H + v * 8,
                    make_uint2(pack_e4m3x4(q[0], q[1], q[2], q[3]),
                               pack_e4m3x4(q[4], q[5], q[6], q[7])));
@@ -502,7 +560,7 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
     uint8_t* sf_row = static_cast<uint8_t*>(p.out_scales) + scale_row_base(p, t);
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
-      const int v = c + k * p.nthreads;
+      const int v = v0 + c + k * p.nthreads;
       float y[8];
       float amax = 0.0f;
 #pragma unroll
@@ -516,25 +574,27 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
       const float mult = sfv == 0.0f ? 0.0f : qc.gs / sfv;
 #pragma unroll
       for (int e = 0; e < 8; ++e) y[e] *= mult;
-      if (v < p.nvec) {
+      if (v < vlim) {
         stg_stream(static_cast<uint8_t*>(p.out) + t * (H / 2) + v * 4, pack_e2m1x8(y));
         if ((v & 1) == 0) sf_row[scale_col_offset(p, v >> 1)] = static_cast<uint8_t>(sf);
-      } else if (is_scale_pad_vector(p, v)) {
+      } else if (kSplit == 1 && is_scale_pad_vector(p, v)) {
         sf_row[scale_col_offset(p, v >> 1)] = 0;
       }
     }
+    if (kSplit > 1) zero_scale_pad_columns(p, t, c, v0);
   }
   return abort_all;
 }
 
 // This thread's weight and bias vectors (zero past the row).
-template <int kVec>
+template <int kVec, int kSplit = 1>
 __device__ __forceinline__ void load_row_constants(const Params& p, int c, uint4 (&w)[kVec],
-                                                   uint4 (&b)[kVec]) {
+                                                   uint4 (&b)[kVec], int vbase = 0,
+                                                   int vend = 0) {
 #pragma unroll
   for (int k = 0; k < kVec; ++k) {
-    const int v = c + k * p.nthreads;
-    const bool ok = v < p.nvec;
+    const int v = (kSplit > 1 ? vbase : 0) + c + k * p.nthreads;
+    const bool ok = v < (kSplit > 1 ? vend : p.nvec);
     w[k] = ok ? ldg_keep(p.weight + v * 8) : make_uint4(0, 0, 0, 0);
     b[k] = (ok && p.bias) ? ldg_keep(p.bias + v * 8) : make_uint4(0, 0, 0, 0);
   }

@@ -193,6 +193,19 @@ int consumer_threads(int64_t H, int vec) {
   return static_cast<int>((per + 31) / 32 * 32);
 }
 
+// Split rows: 16-byte vectors of a row per CTA of the cluster (even, so that an NVFP4 block's two
+// vectors stay in one CTA), and the consumer threads that cover them.
+int split_chunk(int64_t H, int split) {
+  const int64_t nvec = H / 8;
+  const int64_t chunk = (nvec + split - 1) / split;
+  return static_cast<int>((chunk + 1) / 2 * 2);
+}
+int split_threads(int64_t H, int split, int vec) {
+  const int64_t per = (split_chunk(H, split) + vec - 1) / vec;
+  return static_cast<int>((per + 31) / 32 * 32);
+}
+int split_of(const sp_launch_config& cfg) { return cfg.split > 1 ? cfg.split : 1; }
+
 // Dynamic shared memory of the staged kernel: [full barriers][empty barriers][reduction slots]
 // [abort flag, pad] [row index per stage] | weight copy [H] bf16, bias copy [H] bf16 |
 // ring of `stages` segments.
@@ -314,12 +327,52 @@ cudaError_t set_staged_smem_limit(DeviceInfo* dev) {
   return e;
 }
 
+// Split rows: clusters of `split` CTAs (one row each at a time), as many as the SMs hold at the
+// requested CTAs per SM, and never more than rows; launched with PDL like the rest.
+template <int kVec, int kMode, int kSplit>
+cudaError_t launch_split(const sp_launch_config& cfg, const spk::Params& p, cudaStream_t stream,
+                         DeviceInfo* dev) {
+  auto kernel = spk::k_direct<kVec, kMode, kSplit>;
+  int resident = 0;
+  cudaError_t e = resident_ctas(kernel, p.nthreads, 0, dev->id, &resident);
+  if (e != cudaSuccess) return e;
+  if (resident < 1) return cudaErrorInvalidConfiguration;
+  const int per_sm = cfg.ctas_per_sm < resident ? cfg.ctas_per_sm : resident;
+  int64_t clusters = static_cast<int64_t>(dev->sms.load(std::memory_order_relaxed)) * per_sm / kSplit;
+  if (clusters > p.rows_total) clusters = p.rows_total;
+  if (clusters < 1) clusters = 1;
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(static_cast<unsigned>(clusters * kSplit));
+  lc.blockDim = dim3(static_cast<unsigned>(p.nthreads));
+  lc.dynamicSmemBytes = 0;
+  lc.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kSplit;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 2;
+  e = cudaLaunchKernelEx(&lc, kernel, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <int kVec, int kMode>
 cudaError_t launch_one(const sp_launch_config& cfg, spk::Params& p, int smem, int schedule,
                        cudaStream_t stream, DeviceInfo* dev) {
   int grid = 0;
   if (cfg.kernel == SP_KERNEL_DIRECT) {
-    auto kernel = spk::k_direct<kVec, kMode>;
+    if constexpr (kVec <= 2) {
+      switch (split_of(cfg)) {
+        case 2: return launch_split<kVec, kMode, 2>(cfg, p, stream, dev);
+        case 4: return launch_split<kVec, kMode, 4>(cfg, p, stream, dev);
+        case 8: return launch_split<kVec, kMode, 8>(cfg, p, stream, dev);
+        default: break;
+      }
+    }
+    auto kernel = spk::k_direct<kVec, kMode, 1>;
     cudaError_t e = persistent_grid(kernel, p.nthreads, 0, cfg.ctas_per_sm, p.T_pad, dev, &grid);
     if (e != cudaSuccess) return e;
     e = launch_pdl(kernel, grid, p.nthreads, 0, stream, p);
@@ -373,7 +426,14 @@ sp_status config_is_valid(const sp_launch_config& cfg, int64_t H) {
   if (cfg.vec_per_thread != 1 && cfg.vec_per_thread != 2 && cfg.vec_per_thread != 4)
     return SP_ERR_INVALID_ARG;
   if (cfg.ctas_per_sm < 1 || cfg.ctas_per_sm > 32) return SP_ERR_INVALID_ARG;
-  if (consumer_threads(H, cfg.vec_per_thread) > spk::kMaxConsumerThreads) return SP_ERR_UNSUPPORTED;
+  if (cfg.split != 0 && cfg.split != 1 && cfg.split != 2 && cfg.split != 4 && cfg.split != 8)
+    return SP_ERR_INVALID_ARG;
+  const int split = split_of(cfg);
+  if (split > 1 && (cfg.kernel != SP_KERNEL_DIRECT || cfg.vec_per_thread > 2))
+    return SP_ERR_UNSUPPORTED;
+  const int threads = split > 1 ? split_threads(H, split, cfg.vec_per_thread)
+                                : consumer_threads(H, cfg.vec_per_thread);
+  if (threads > spk::kMaxConsumerThreads) return SP_ERR_UNSUPPORTED;
   if (cfg.kernel == SP_KERNEL_STAGED) {
     const int most = max_stages(H, cfg.ctas_per_sm);
     if (cfg.stages < 0 || cfg.stages > most || most < 2 || cfg.stages == 1)
@@ -417,6 +477,10 @@ sp_status run_checked(const sp_launch_config& cfg_in, const void* partials, int 
   p.nvec = static_cast<int>(H / 8);
   p.tp = tp;
   p.nthreads = consumer_threads(H, cfg.vec_per_thread);
+  if (split_of(cfg) > 1) {
+    p.split_chunk = split_chunk(H, split_of(cfg));
+    p.nthreads = split_threads(H, split_of(cfg), cfg.vec_per_thread);
+  }
   p.eps = eps;
   int smem = 0;
   if (cfg.kernel == SP_KERNEL_STAGED) {
@@ -608,6 +672,7 @@ void sp_options_init(sp_fused_options* options) {
   options->scale_layout = SP_SCALES_ROW_MAJOR;
   options->host_buffers = 0;
   options->schedule = SP_SCHEDULE_AUTO;
+  options->launch = nullptr;
 }
 
 sp_status sp_fused_reduce_norm_ex(const sp_fused_options* options, const void* partials, int tp,
@@ -627,12 +692,21 @@ sp_status sp_fused_reduce_norm_ex(const sp_fused_options* options, const void* p
                        scale, out, out_scales, residual_out, x);
   if (st != SP_OK) return st;
   if (o.host_buffers != 0 && o.host_buffers != 1) return SP_ERR_UNSUPPORTED;
+  if (o.launch) {
+    st = config_is_valid(*o.launch, H);
+    if (st != SP_OK) return st;
+    if (o.host_buffers && o.launch->kernel != SP_KERNEL_DIRECT) return SP_ERR_UNSUPPORTED;
+  }
   if (T_pad == 0) return SP_OK;
   const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!o.host_buffers) {
     sp_launch_config cfg;
-    st = sp_select_launch(tp, T_pad, H, quant_mode, &cfg);
-    if (st != SP_OK) return st;
+    if (o.launch) {
+      cfg = *o.launch;
+    } else {
+      st = sp_select_launch(tp, T_pad, H, quant_mode, &cfg);
+      if (st != SP_OK) return st;
+    }
     return run_checked(cfg, partials, tp, T_pad, T_valid, H, residual, weight, bias, eps,
                        quant_mode, scale, out, out_scales, residual_out, s, x);
   }
@@ -649,6 +723,7 @@ sp_status sp_fused_reduce_norm_ex(const sp_fused_options* options, const void* p
   cfg.vec_per_thread = consumer_threads(H, 2) > spk::kMaxConsumerThreads ? 4 : 2;
   cfg.ctas_per_sm = 4;
   cfg.stages = 0;
+  if (o.launch) cfg = *o.launch;
   x.addend = dev[8];
   return run(cfg, dev[0], tp, T_pad, T_valid, H, dev[1], dev[2], dev[3], eps, quant_mode,
              static_cast<const float*>(dev[4]), const_cast<void*>(dev[5]),
@@ -680,10 +755,15 @@ sp_status sp_check_args_ex(const sp_fused_options* options, const void* partials
   x.addend = o.addend;
   x.scale_layout = o.scale_layout;
   x.schedule = o.schedule;
-  const sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps,
-                             quant_mode, scale, out, out_scales, residual_out, x);
+  sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode,
+                       scale, out, out_scales, residual_out, x);
   if (st != SP_OK) return st;
   if (o.host_buffers != 0 && o.host_buffers != 1) return SP_ERR_UNSUPPORTED;
+  if (o.launch) {
+    st = config_is_valid(*o.launch, H);
+    if (st != SP_OK) return st;
+    if (o.host_buffers && o.launch->kernel != SP_KERNEL_DIRECT) return SP_ERR_UNSUPPORTED;
+  }
   return SP_OK;
 }
 

@@ -274,22 +274,31 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
 }
 
 // ----------------------------------------------------------------------------------- direct
-template <int kVec, int kMode>
+// kSplit > 1: each row is split across the kSplit CTAs of a thread-block cluster, CTA r owning
+// vectors [r * split_chunk, (r + 1) * split_chunk) of it; the CTAs combine the row's sum of
+// squares (and max) through distributed shared memory. A call with few rows then draws on
+// kSplit times as many SMs.
+template <int kVec, int kMode, int kSplit>
 __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) {
   __shared__ RedSlot slots[64];
+  __shared__ float2 cslots[2];
   const int c = threadIdx.x;
   const int nc = p.nthreads;
   const int64_t H = p.H;
+  const int vbase = kSplit > 1 ? cluster_rank() * p.split_chunk : 0;
+  const int vend = kSplit > 1 ? min(vbase + p.split_chunk, p.nvec) : p.nvec;
+  const int vc = vbase + c;  // this thread's first vector
   pdl_launch_dependents();
   pdl_wait_prerequisites();
   uint4 w[kVec], b[kVec];
-  load_row_constants<kVec>(p, c, w, b);
+  load_row_constants<kVec, kSplit>(p, c, w, b, vbase, vend);
   const QuantConst qc = load_quant_const<kMode>(p);
 
   int parity = 0;
-  for (int64_t t = blockIdx.x; t < p.rows_total; t += gridDim.x) {
+  // every CTA of a cluster takes the same rows, so all meet the same cluster barriers
+  for (int64_t t = blockIdx.x / kSplit; t < p.rows_total; t += gridDim.x / kSplit) {
     if (t >= p.T_valid) {
-      zero_row<kVec, kMode>(p, t, c);
+      zero_row<kVec, kMode, kSplit>(p, t, c, vbase, vend);
       continue;
     }
     float h[kVec][8];
@@ -306,8 +315,8 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
       for (int u = 0; u < 4; ++u)
 #pragma unroll
         for (int k = 0; k < kVec; ++k) {
-          const int v = c + k * nc;
-          x[u][k] = v < p.nvec ? ldg_stream(row + (r + u) * p.plane + v * 8) : make_uint4(0, 0, 0, 0);
+          const int v = vc + k * nc;
+          x[u][k] = v < vend ? ldg_stream(row + (r + u) * p.plane + v * 8) : make_uint4(0, 0, 0, 0);
         }
 #pragma unroll
       for (int u = 0; u < 4; ++u)
@@ -317,8 +326,8 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
     for (; r < p.tp; ++r) {
 #pragma unroll
       for (int k = 0; k < kVec; ++k) {
-        const int v = c + k * nc;
-        if (v < p.nvec) add_bf16x8(ldg_stream(row + r * p.plane + v * 8), h[k]);
+        const int v = vc + k * nc;
+        if (v < vend) add_bf16x8(ldg_stream(row + r * p.plane + v * 8), h[k]);
       }
     }
     if (p.partial_scale != 1.0f) {
@@ -328,22 +337,24 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
     if (p.residual) {
 #pragma unroll
       for (int k = 0; k < kVec; ++k) {
-        const int v = c + k * nc;
-        if (v < p.nvec) add_bf16x8(ldg_stream(p.residual + t * H + v * 8), h[k]);
+        const int v = vc + k * nc;
+        if (v < vend) add_bf16x8(ldg_stream(p.residual + t * H + v * 8), h[k]);
       }
     }
     if (p.addend) {
 #pragma unroll
       for (int k = 0; k < kVec; ++k) {
-        const int v = c + k * nc;
-        if (v < p.nvec) add_bf16x8(ldg_stream(p.addend + t * H + v * 8), h[k]);
+        const int v = vc + k * nc;
+        if (v < vend) add_bf16x8(ldg_stream(p.addend + t * H + v * 8), h[k]);
       }
     }
 #pragma unroll
     for (int k = 0; k < kVec; ++k) add_bf16x8(b[k], h[k]);
-    finish_row<kVec, kMode>(p, t, h, w, qc, slots, parity, c, 0);
+    finish_row<kVec, kMode, kSplit>(p, t, h, w, qc, slots, parity, c, 0, vbase, vend, cslots);
     parity ^= 1;
   }
+  // No CTA leaves while another CTA of its cluster may still read its cslots.
+  if constexpr (kSplit > 1) cluster_sync();
 }
 
 // ----------------------------------------------------------------------------------- self-test

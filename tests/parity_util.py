@@ -124,9 +124,8 @@ def run_gpu(inp: dict, *, config: dict | None = None, fill: int = 0xA5, inplace:
               out_scales=sc, T_valid=inp["T_valid"], stream=stream)
     if (partial_scale != 1.0 or inp.get("addend") is not None or scale_layout != 0
             or schedule != "auto"):
-        assert config is None
         opts = sp.sp_options_init(partial_scale=partial_scale, addend=inp.get("addend"),
-                                  scale_layout=scale_layout, schedule=schedule)
+                                  scale_layout=scale_layout, schedule=schedule, launch=config)
         sp.sp_fused_reduce_norm_ex(opts, inp["partials"], inp["weight"], out, res_out, **kw)
     elif config is None:
         sp.sp_fused_reduce_norm(inp["partials"], inp["weight"], out, res_out, **kw)

@@ -239,6 +239,34 @@ OPTION_CASES = [
     (dict(schedule=3), {}, "SP_ERR_UNSUPPORTED"),
     (dict(schedule=-1), {}, "SP_ERR_UNSUPPORTED"),
     (dict(addend=A * 20), {"T_pad": 18}, "SP_ERR_INVALID_ARG"),     # shape rule first
+    # an explicit launch configuration: the checks of sp_fused_reduce_norm_with_config
+    (dict(launch=dict(kernel=1, vec_per_thread=1, ctas_per_sm=4)), {}, "SP_OK"),
+    (dict(launch=dict(kernel=0, vec_per_thread=2, ctas_per_sm=2, stages=3)), {}, "SP_OK"),
+    (dict(launch=dict(kernel=2, vec_per_thread=1, ctas_per_sm=4)), {}, "SP_ERR_INVALID_ARG"),
+    (dict(launch=dict(kernel=1, vec_per_thread=3, ctas_per_sm=4)), {}, "SP_ERR_INVALID_ARG"),
+    (dict(launch=dict(kernel=1, vec_per_thread=1, ctas_per_sm=0)), {}, "SP_ERR_INVALID_ARG"),
+    (dict(launch=dict(kernel=0, vec_per_thread=2, ctas_per_sm=2, stages=1)), {},
+     "SP_ERR_UNSUPPORTED"),
+    # split rows: 0/1 (whole rows), 2, 4, 8 with the direct kernel and 1-2 vectors per thread
+    (dict(launch=dict(kernel=1, vec_per_thread=1, ctas_per_sm=4, split=1)), {}, "SP_OK"),
+    (dict(launch=dict(kernel=1, vec_per_thread=1, ctas_per_sm=4, split=2)), {}, "SP_OK"),
+    (dict(launch=dict(kernel=1, vec_per_thread=2, ctas_per_sm=4, split=4)), {}, "SP_OK"),
+    (dict(launch=dict(kernel=1, vec_per_thread=1, ctas_per_sm=4, split=8)), {}, "SP_OK"),
+    (dict(launch=dict(kernel=1, vec_per_thread=1, ctas_per_sm=4, split=3)), {},
+     "SP_ERR_INVALID_ARG"),
+    (dict(launch=dict(kernel=1, vec_per_thread=1, ctas_per_sm=4, split=16)), {},
+     "SP_ERR_INVALID_ARG"),
+    (dict(launch=dict(kernel=1, vec_per_thread=1, ctas_per_sm=4, split=-2)), {},
+     "SP_ERR_INVALID_ARG"),
+    (dict(launch=dict(kernel=1, vec_per_thread=4, ctas_per_sm=4, split=2)), {},
+     "SP_ERR_UNSUPPORTED"),
+    (dict(launch=dict(kernel=0, vec_per_thread=2, ctas_per_sm=2, stages=3, split=2)), {},
+     "SP_ERR_UNSUPPORTED"),
+    (dict(launch=dict(kernel=1, vec_per_thread=1, ctas_per_sm=4, split=8), scale_layout=1),
+     {"quant_mode": "nvfp4", "scale": A * 14}, "SP_OK"),
+    (dict(launch=dict(kernel=1, vec_per_thread=2, ctas_per_sm=4), host_buffers=1), {}, "SP_OK"),
+    (dict(launch=dict(kernel=0, vec_per_thread=2, ctas_per_sm=2, stages=3), host_buffers=1), {},
+     "SP_ERR_UNSUPPORTED"),
 ]
 
 
@@ -248,8 +276,14 @@ def test_option_checks(lib, opt, kw, want):
     lib.sp_options_init(ctypes.byref(o))
     assert o.partial_scale == 1.0 and o.addend is None and o.scale_layout == 0
     assert o.host_buffers == 0 and o.schedule == 0  # SP_SCHEDULE_AUTO
+    assert not o.launch  # NULL: the library's own choice
+    cfg = None
     for k, v in opt.items():
-        setattr(o, k, v)
+        if k == "launch":
+            cfg = sp.LaunchConfig(**v)
+            o.launch = ctypes.pointer(cfg)
+        else:
+            setattr(o, k, v)
     a = {**_base(), **kw}
     st = sp.sp_check_args_ex(o, a["partials"], a["tp"], a["T_pad"], a["T_valid"], a["H"],
                              a["residual"], a["weight"], a["bias"], a["eps"], a["quant_mode"],

@@ -616,3 +616,83 @@ def test_default_launch_in_each_band(tp, T, H, mode, band):
     w = dict(synth.workload(3), mode=mode, scale=0.05 if mode == "fp8_static" else None)
     inp = synth.make_inputs(w, device=DEV, tp=tp, T_pad=T, T_valid=T - 3, H=H)
     assert _check(inp)
+
+
+# ------------------------------------------------------------------------- split rows
+def _split_cfg(split, vec, ctas=2):
+    return dict(kernel=1, vec_per_thread=vec, ctas_per_sm=ctas, stages=0, split=split)
+
+
+@pytest.mark.parametrize("mode", ["none", "fp8_static", "fp8_per_token", "nvfp4"])
+@pytest.mark.parametrize("split,vec", [(2, 1), (2, 2), (4, 1), (4, 2), (8, 1), (8, 2)])
+@pytest.mark.parametrize("tp,T,H", [(8, 16, 8192), (4, 40, 4096), (3, 24, 1040), (2, 10, 16)])
+def test_split_rows(mode, split, vec, tp, T, H):
+    """Rows split across the CTAs of a cluster: every slice size, including CTAs whose slice is
+    empty (H = 16 at split 8) and slices that end mid-warp (H = 1040)."""
+    w = dict(synth.workload(3), mode=mode, scale=0.05 if mode == "fp8_static" else None)
+    inp = synth.make_inputs(w, device=DEV, tp=tp, T_pad=T, T_valid=T - 3, H=H)
+    assert _check(inp, config=_split_cfg(split, vec))
+
+
+@pytest.mark.parametrize("split,ctas", [(8, 1), (4, 1), (2, 1)])
+def test_split_rows_many_rows_per_cluster(split, ctas):
+    """Fewer clusters than rows: each cluster takes several rows in turn, reusing its two
+    cross-CTA reduction slots on alternate rows."""
+    w = synth.workload(4)  # per-token FP8 (the row max crosses the cluster too)
+    inp = _small(w, rows=1000, H=2048)
+    assert _check(inp, config=_split_cfg(split, 1, ctas))
+
+
+@pytest.mark.parametrize("mode", ["none", "fp8_static", "fp8_per_token", "nvfp4"])
+@pytest.mark.parametrize("split", [2, 8])
+def test_split_rows_with_options(mode, split):
+    """Split rows with a partial scale, an addend and (NVFP4) the swizzled scale layout, whose
+    padding rows and columns the cluster's first CTA must zero."""
+    w = dict(synth.workload(3), mode=mode, scale=0.05 if mode == "fp8_static" else None)
+    inp = synth.make_inputs(w, device=DEV, tp=4, T_pad=24, T_valid=21, H=1040, with_addend=True)
+    layout = 1 if mode == "nvfp4" else 0
+    kw = dict(config=_split_cfg(split, 1), partial_scale=0.5, scale_layout=layout)
+    a = run_gpu(inp, fill=0xA5, **kw)
+    b = run_gpu(inp, fill=0x5A, **kw)
+    for k in ("out", "out_scales", "residual_out"):
+        if a[k] is not None:
+            assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+    compare(a, run_oracle(inp, partial_scale=0.5, scale_layout=layout), inp)
+
+
+def test_split_rows_captured_in_a_graph_after_other_kernels():
+    """Split-row launches (clusters with the programmatic-dependent-launch attribute) inside a
+    CUDA graph, each after a PyTorch kernel that rewrites its partials: every replay computes on
+    the new contents."""
+    w = synth.workload(4)
+    inp = synth.make_inputs(w, device=DEV, tp=8, T_pad=16, T_valid=13, H=8192)
+    outs = sp.allocate_outputs(inp["T_pad"], inp["H"], inp["mode"], DEV)
+    src = inp["partials"].clone()
+    opts = sp.sp_options_init(launch=_split_cfg(8, 1))
+    s = torch.cuda.Stream(device=DEV)
+
+    def step():
+        inp["partials"].copy_(src)
+        inp["partials"].mul_(0.5)
+        sp.sp_fused_reduce_norm_ex(opts, inp["partials"], inp["weight"], outs["out"],
+                                   outs["residual_out"], residual=inp["residual"],
+                                   bias=inp["bias"], eps=inp["eps"], quant_mode=inp["mode"],
+                                   out_scales=outs["out_scales"], T_valid=inp["T_valid"])
+
+    with torch.cuda.stream(s):
+        step()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        step()
+        step()
+    fresh = synth.make_inputs(w, device=DEV, tp=8, T_pad=16, T_valid=13, H=8192,
+                              seed=inp["seed"] + 9)
+    src.copy_(fresh["partials"])
+    for k in ("residual", "weight", "bias"):
+        inp[k].copy_(fresh[k])
+    torch.cuda.synchronize()
+    g.replay()
+    torch.cuda.synchronize()
+    fresh["partials"] = (fresh["partials"].float() * 0.5).to(torch.bfloat16)
+    compare(_host(outs), run_oracle(fresh), fresh)

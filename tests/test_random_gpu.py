@@ -1,5 +1,5 @@
-"""GPU parity on seeded random problems: shapes, modes, optional inputs, options and launch
-configurations and row schedules drawn together, so that combinations the hand-picked cases do not list are
+"""GPU parity on seeded random problems: shapes, modes, optional inputs, options, launch
+configurations (split rows included) and row schedules drawn together, so that combinations the hand-picked cases do not list are
 covered too. Each problem is compared with the oracle element by element under the tolerances
 of parity_util, after two runs into differently pre-filled, guard-banded outputs. Random
 FlashComm2 reorganisations are compared byte for byte.
@@ -49,17 +49,18 @@ def _draw(i: int) -> dict:
         p["schedule"] = r.choice(["static", "dynamic"])
     options = (p["with_addend"] or p["partial_scale"] != 1.0 or p["scale_layout"] != 0
                or p["schedule"] != "auto")
-    if not options:
-        if p["with_residual"] and r.random() < 0.2:
-            p["inplace"] = True
-        if r.random() < 0.6:
-            kernel = r.choice([0, 1])
-            vec = r.choice([1, 2, 4])
-            while -(-(H // 8) // vec) > 512:
-                vec *= 2
-            if vec <= 4:
-                p["config"] = dict(kernel=kernel, vec_per_thread=vec, ctas_per_sm=r.randint(1, 8),
-                                   stages=r.choice([0, 2, 3, 4]) if kernel == 0 else 0)
+    if not options and p["with_residual"] and r.random() < 0.2:
+        p["inplace"] = True
+    if r.random() < 0.6:  # a forced launch (passed in the options when there are any)
+        kernel = r.choice([0, 1])
+        vec = r.choice([1, 2, 4])
+        while -(-(H // 8) // vec) > 512:
+            vec *= 2
+        if vec <= 4:
+            p["config"] = dict(kernel=kernel, vec_per_thread=vec, ctas_per_sm=r.randint(1, 8),
+                               stages=r.choice([0, 2, 3, 4]) if kernel == 0 else 0)
+            if kernel == 1 and vec <= 2 and r.random() < 0.5:
+                p["config"]["split"] = r.choice([2, 4, 8])
     return p
 
 
@@ -106,6 +107,11 @@ def test_draws_cover_every_mode_and_option():
     assert any(not p["with_residual"] for p in ps) and any(not p["with_bias"] for p in ps)
     assert any(p["T_valid"] < p["T_pad"] for p in ps)
     assert {p["schedule"] for p in ps} == {"auto", "static", "dynamic"}
+    splits = [p for p in ps if p["config"] and p["config"].get("split", 0) > 1]
+    assert {p["config"]["split"] for p in splits} == {2, 4, 8}
+    assert {p["mode"] for p in splits} == set(MODES)
+    assert any(p["scale_layout"] == 1 for p in splits)
+    assert any(p["config"] and p["with_addend"] for p in ps)
 
 
 def _draw_fc2(i: int) -> dict:
