@@ -547,15 +547,25 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   // direct kernel (no ring to set up; loads four partials at a time) is fastest while its loads
   // fit in one wave; the staged kernel's floor grows with the row's segment count (each passes
   // through the ring in turn), but it keeps all of a row's segments in flight with a deep ring.
-  // From a GB300 sweep of tp 2-16, H 1024-8192, T 8-4096 (call time):
-  //   H <= 4096, T <= 256: direct below ~1.5M partial elements for tp <= 4 (2M for larger tp),
-  //                        else the staged kernel at 2 CTAs/SM with as many stages as fit
-  //                        (7-27 % faster than either previous choice);
-  //   H <= 4096, T > 256:  direct while T * H <= 2^20 (2^22 for H <= 1024, where a row's
-  //                        2 KB segments leave the ring little to hide: 10-35 % faster);
-  //   4096 < H <= 8192:    direct while tp * T * H <= 2^20 (13-30 % faster at T = 8-64);
-  //                        for 64-128 rows, the staged kernel at one CTA per SM with every
-  //                        stage that fits (a 12-stage ring at H = 8192: 10-34 % faster);
+  // With only a few rows, one SM per row caps the call at what an SM can pull in (about
+  // 45 GB/s): splitting each row across a cluster of 4 or 8 CTAs draws on that many more SMs.
+  // From GB300 sweeps of tp 2-16, H 1024-16384, T 1-4096 (call time, launches replayed from a
+  // CUDA graph and single launches):
+  //   H <= 4096, tp <= 5, T <= 256: direct below ~1.5M partial elements for tp <= 4 (2M for
+  //                        tp = 5), else the staged kernel at 2 CTAs/SM with as many stages as
+  //                        fit (7-27 % faster than either previous choice);
+  //   H <= 4096 otherwise: direct while T * H <= 2^20 (2^22 for H <= 1024, where a row's 2 KB
+  //                        segments leave the ring little to hide: 10-35 % faster; at tp >= 8
+  //                        and T <= 256, 13-70 % faster than the deep ring);
+  //   4096 < H <= 8192:    split rows (one vector per thread) for few rows: tp >= 12, 8 CTAs
+  //                        per row up to 16 rows and 4 up to 64 (10-100 % faster); 6 <= tp < 12,
+  //                        8 up to 8 rows and 4 up to 32 (5-32 %); tp 2-5 at H >= 7168, 8 up to
+  //                        8 rows (0-10 %); split rows lost at H <= 4096. Otherwise direct while
+  //                        tp * T * H <= 2^20 (13-30 % faster at T = 8-64); for 64-128 rows, the
+  //                        staged kernel at one CTA per SM with every stage that fits (a 12-stage
+  //                        ring at H = 8192: 10-34 % faster);
+  //   H > 8192:            direct (four vectors per thread) up to 32 rows for tp <= 8, 16 rows
+  //                        above (7-56 % faster than the staged kernel);
   //   4096 < H <= 6144, more rows than SMs but no more than one round of the large-call grid:
   //                        ceil(T / SMs) CTAs per SM, every stage that fits (6-27 % faster at
   //                        T = 160-456; at H = 4096 and from 7168 up it was a wash);
@@ -566,22 +576,32 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   bool direct = false;
   bool deep_ring = false;
   bool deep_ring_1 = false;
+  int split = 0;
   if (H <= 4096) {
-    if (T_pad <= 256) {
+    if (T_pad <= 256 && tp <= 5) {
       direct = tp <= 4 ? elems < 3 * (int64_t{1} << 19) : elems <= (int64_t{1} << 21);
       deep_ring = !direct;
     } else {
       direct = T_pad * H <= (int64_t{1} << (H <= 1024 ? 22 : 20));
     }
   } else if (H <= 8192) {
-    direct = elems <= (int64_t{1} << 20);
+    if (tp >= 12)
+      split = T_pad <= 16 ? 8 : (T_pad <= 64 ? 4 : 0);
+    else if (tp >= 6)
+      split = T_pad <= 8 ? 8 : (T_pad <= 32 ? 4 : 0);
+    else if (tp >= 2 && H >= 7168)
+      split = T_pad <= 8 ? 8 : 0;
+    direct = split > 0 || elems <= (int64_t{1} << 20);
     deep_ring_1 = !direct && T_pad >= 64 && T_pad <= 128;
+  } else {
+    direct = T_pad <= (tp <= 8 ? 32 : 16);
   }
   if (direct) {
     c.kernel = SP_KERNEL_DIRECT;
-    c.vec_per_thread = H <= 4096 ? 1 : 2;
+    c.vec_per_thread = (split > 0 || H <= 4096) ? 1 : (H <= 8192 ? 2 : 4);
     c.ctas_per_sm = H <= 4096 ? 16 : 8;
     c.stages = 0;
+    c.split = split;
   } else if (deep_ring && c.kernel == SP_KERNEL_STAGED && max_stages(H, 2) >= c.stages) {
     c.ctas_per_sm = 2;
     c.stages = 0;  // as many as fit

@@ -103,12 +103,30 @@ def test_launch_selection(lib):
     (4, 64, 4096, (1, 1, 16, 0)),       # 1M partial elements, tp <= 4: direct
     (4, 128, 4096, (0, 2, 2, 0)),       # 2M, few rows: staged, deep ring at 2 CTAs/SM
     (8, 64, 4096, (1, 1, 16, 0)),       # 2M, tp > 4: direct
-    (16, 64, 4096, (0, 2, 2, 0)),       # 4M: deep ring
+    (16, 64, 4096, (1, 1, 16, 0)),      # tp >= 6: direct while T * H <= 2^20
+    (16, 256, 2048, (1, 1, 16, 0)),
+    (5, 160, 4096, (0, 2, 2, 0)),       # tp = 5: deep ring above 2M partial elements
     (8, 512, 2048, (1, 1, 16, 0)),      # T > 256: direct while T * H <= 2^20
     (4, 4096, 1024, (1, 1, 16, 0)),     # ... 2^22 for H <= 1024
     (4, 8192, 1024, (0, 2, 16, 4)),
     (4, 32, 8192, (1, 2, 8, 0)),        # 4096 < H <= 8192: direct while tp*T*H <= 2^20
-    (8, 32, 8192, (0, 2, 2, 4)),        # 2M: the staged kernel
+    (4, 64, 8192, (0, 2, 1, 0)),        # 2M: the staged kernel
+    # split rows: a cluster of 8 or 4 CTAs per row, one vector per thread
+    (8, 8, 8192, (1, 1, 8, 0, 8)),
+    (8, 32, 5120, (1, 1, 8, 0, 4)),
+    (8, 40, 5120, (0, 2, 3, 4)),        # more rows: no split
+    (16, 16, 7168, (1, 1, 8, 0, 8)),
+    (16, 64, 8192, (1, 1, 8, 0, 4)),
+    (16, 80, 8192, (0, 2, 1, 0)),
+    (2, 8, 7168, (1, 1, 8, 0, 8)),
+    (4, 8, 5120, (1, 2, 8, 0)),         # tp < 6 splits only from H = 7168
+    (4, 16, 8192, (1, 2, 8, 0)),
+    (8, 8, 4096, (1, 1, 16, 0)),        # never at H <= 4096
+    (1, 8, 8192, (1, 2, 8, 0)),
+    # H > 8192: direct with four vectors per thread for few rows
+    (2, 32, 16384, (1, 4, 8, 0)),
+    (16, 16, 16384, (1, 4, 8, 0)),
+    (16, 32, 16384, (0, 4, 1, 4)),
     (8, 64, 8192, (0, 2, 1, 0)),        # 64-128 rows: one CTA per SM, deepest ring
     (16, 128, 7168, (0, 2, 1, 0)),
     (16, 256, 7168, (0, 2, 2, 4)),
@@ -125,7 +143,8 @@ def test_launch_selection(lib):
 ])
 def test_launch_rule(lib, tp, T, H, want):
     c = sp.sp_select_launch(tp, T, H, "none")
-    assert (c.kernel, c.vec_per_thread, c.ctas_per_sm, c.stages) == want
+    want = tuple(want) + (0,) * (5 - len(want))
+    assert (c.kernel, c.vec_per_thread, c.ctas_per_sm, c.stages, c.split) == want
 
 
 A = 1 << 20  # fake 16-byte-aligned addresses: compared, never dereferenced

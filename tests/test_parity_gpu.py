@@ -601,7 +601,11 @@ def test_dynamic_schedule_soak_two_chained_streams():
 # ------------------------------------------------------------------------- launch-rule bands
 @pytest.mark.parametrize("tp,T,H,mode,band", [
     (4, 32, 8192, "fp8_per_token", (1, 2, 8, 0)),     # direct, two vectors per thread
-    (16, 64, 4096, "none", (0, 2, 2, 0)),             # staged, deep ring at 2 CTAs/SM
+    (4, 128, 4096, "none", (0, 2, 2, 0)),             # staged, deep ring at 2 CTAs/SM
+    (16, 128, 2048, "fp8_static", (1, 1, 16, 0)),     # direct at tp >= 6
+    (16, 16, 8192, "fp8_per_token", (1, 1, 8, 0, 8)), # split rows, 8 CTAs per row
+    (8, 32, 5120, "nvfp4", (1, 1, 8, 0, 4)),          # split rows, 4 CTAs per row
+    (2, 24, 16384, "fp8_static", (1, 4, 8, 0)),       # direct, four vectors per thread
     (8, 96, 7168, "nvfp4", (0, 2, 1, 0)),             # staged, one CTA per SM
     (8, 256, 5120, "fp8_static", (0, 2, 2, 0)),       # one round of rows, fewest CTAs
     (4, 768, 4096, "none", (0, 2, 3, 0)),             # last round filled at 3 CTAs/SM
@@ -612,7 +616,8 @@ def test_dynamic_schedule_soak_two_chained_streams():
 def test_default_launch_in_each_band(tp, T, H, mode, band):
     """Each band of the launch rule, checked to be the band and compared with the oracle."""
     c = sp.sp_select_launch(tp, T, H, mode)
-    assert (c.kernel, c.vec_per_thread, c.ctas_per_sm, c.stages) == band
+    band = tuple(band) + (0,) * (5 - len(band))
+    assert (c.kernel, c.vec_per_thread, c.ctas_per_sm, c.stages, c.split) == band
     w = dict(synth.workload(3), mode=mode, scale=0.05 if mode == "fp8_static" else None)
     inp = synth.make_inputs(w, device=DEV, tp=tp, T_pad=T, T_valid=T - 3, H=H)
     assert _check(inp)
