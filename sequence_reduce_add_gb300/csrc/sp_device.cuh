@@ -491,10 +491,16 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
   const int v0 = kSplit > 1 ? vbase : 0;
   const int vlim = kSplit > 1 ? vend : p.nvec;
   float ss0 = 0.0f, ss1 = 0.0f;  // sums of squares of the even and the odd elements
+  // Split rows: the new residual is stored after the cluster barrier, whose release would
+  // otherwise wait for these stores to complete.
+  uint4 res[kSplit > 1 ? kVec : 1];
 #pragma unroll
   for (int k = 0; k < kVec; ++k) {
     const int v = v0 + c + k * p.nthreads;
-    if (v < vlim) stg_stream(p.residual_out + t * H + v * 8, pack_bf16x8(h[k]));
+    if constexpr (kSplit > 1)
+      res[k] = pack_bf16x8(h[k]);
+    else if (v < vlim)
+      stg_stream(p.residual_out + t * H + v * 8, pack_bf16x8(h[k]));
 #pragma unroll
     for (int e = 0; e < 8; e += 2) fma2(ss0, ss1, h[k][e], h[k][e + 1], h[k][e], h[k][e + 1]);
   }
@@ -514,7 +520,14 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
   int abort_all = 0;
   float2 red =
       row_reduce<kMode == kModeFp8PerToken>(ss, mx, abort, slots, parity, p.nthreads, &abort_all);
-  if constexpr (kSplit > 1) red = cluster_row_sum<kSplit>(red, cslots, parity);
+  if constexpr (kSplit > 1) {
+    red = cluster_row_sum<kSplit>(red, cslots, parity);
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int v = v0 + c + k * p.nthreads;
+      if (v < vlim) stg_stream(p.residual_out + t * H + v * 8, res[k]);
+    }
+  }
   const float rinv = rsqrtf(red.x / static_cast<float>(p.H) + p.eps);
 
   if (kMode == kModeNone) {

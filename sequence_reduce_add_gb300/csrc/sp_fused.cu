@@ -564,8 +564,10 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   //                        tp * T * H <= 2^20 (13-30 % faster at T = 8-64); for 64-128 rows, the
   //                        staged kernel at one CTA per SM with every stage that fits (a 12-stage
   //                        ring at H = 8192: 10-34 % faster);
-  //   H > 8192:            direct (four vectors per thread) up to 32 rows for tp <= 8, 16 rows
-  //                        above (7-56 % faster than the staged kernel);
+  //   H > 8192:            split rows, 8 CTAs per row, one vector per thread: up to 64 rows for
+  //                        tp >= 12, 32 for 6 <= tp < 12, 16 for tp 2-5 (2-85 % faster); else
+  //                        direct (four vectors per thread) up to 32 rows (7-35 % faster than
+  //                        the staged kernel; at 64 rows it was 3-11 % slower);
   //   4096 < H <= 6144, more rows than SMs but no more than one round of the large-call grid:
   //                        ceil(T / SMs) CTAs per SM, every stage that fits (6-27 % faster at
   //                        T = 160-456; at H = 4096 and from 7168 up it was a wash);
@@ -594,7 +596,13 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     direct = split > 0 || elems <= (int64_t{1} << 20);
     deep_ring_1 = !direct && T_pad >= 64 && T_pad <= 128;
   } else {
-    direct = T_pad <= (tp <= 8 ? 32 : 16);
+    if (tp >= 12)
+      split = T_pad <= 64 ? 8 : 0;
+    else if (tp >= 6)
+      split = T_pad <= 32 ? 8 : 0;
+    else if (tp >= 2)
+      split = T_pad <= 16 ? 8 : 0;
+    direct = split > 0 || T_pad <= 32;
   }
   if (direct) {
     c.kernel = SP_KERNEL_DIRECT;

@@ -123,10 +123,15 @@ def test_launch_selection(lib):
     (4, 16, 8192, (1, 2, 8, 0)),
     (8, 8, 4096, (1, 1, 16, 0)),        # never at H <= 4096
     (1, 8, 8192, (1, 2, 8, 0)),
-    # H > 8192: direct with four vectors per thread for few rows
+    # H > 8192: split rows, else direct with four vectors per thread, for few rows
+    (2, 16, 16384, (1, 1, 8, 0, 8)),
     (2, 32, 16384, (1, 4, 8, 0)),
-    (16, 16, 16384, (1, 4, 8, 0)),
-    (16, 32, 16384, (0, 4, 1, 4)),
+    (4, 32, 12288, (1, 4, 8, 0)),
+    (4, 64, 12288, (0, 4, 1, 4)),
+    (8, 32, 12288, (1, 1, 8, 0, 8)),
+    (8, 64, 16384, (0, 4, 1, 4)),
+    (16, 64, 16384, (1, 1, 8, 0, 8)),
+    (16, 128, 16384, (0, 4, 1, 4)),
     (8, 64, 8192, (0, 2, 1, 0)),        # 64-128 rows: one CTA per SM, deepest ring
     (16, 128, 7168, (0, 2, 1, 0)),
     (16, 256, 7168, (0, 2, 2, 4)),

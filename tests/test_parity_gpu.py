@@ -606,6 +606,7 @@ def test_dynamic_schedule_soak_two_chained_streams():
     (16, 16, 8192, "fp8_per_token", (1, 1, 8, 0, 8)), # split rows, 8 CTAs per row
     (8, 32, 5120, "nvfp4", (1, 1, 8, 0, 4)),          # split rows, 4 CTAs per row
     (2, 24, 16384, "fp8_static", (1, 4, 8, 0)),       # direct, four vectors per thread
+    (16, 48, 12288, "nvfp4", (1, 1, 8, 0, 8)),        # split rows at H > 8192
     (8, 96, 7168, "nvfp4", (0, 2, 1, 0)),             # staged, one CTA per SM
     (8, 256, 5120, "fp8_static", (0, 2, 2, 0)),       # one round of rows, fewest CTAs
     (4, 768, 4096, "none", (0, 2, 3, 0)),             # last round filled at 3 CTAs/SM
@@ -636,6 +637,15 @@ def test_split_rows(mode, split, vec, tp, T, H):
     empty (H = 16 at split 8) and slices that end mid-warp (H = 1040)."""
     w = dict(synth.workload(3), mode=mode, scale=0.05 if mode == "fp8_static" else None)
     inp = synth.make_inputs(w, device=DEV, tp=tp, T_pad=T, T_valid=T - 3, H=H)
+    assert _check(inp, config=_split_cfg(split, vec))
+
+
+@pytest.mark.parametrize("mode", ["none", "fp8_per_token", "nvfp4"])
+@pytest.mark.parametrize("split,vec", [(2, 2), (4, 1), (4, 2), (8, 1), (8, 2)])
+def test_split_rows_longest_hidden(mode, split, vec):
+    """Split rows at the largest H the kernels take (16384: 256-1024 vectors per CTA)."""
+    w = dict(synth.workload(3), mode=mode, scale=None)
+    inp = synth.make_inputs(w, device=DEV, tp=4, T_pad=12, T_valid=10, H=sp.sp_max_hidden())
     assert _check(inp, config=_split_cfg(split, vec))
 
 
