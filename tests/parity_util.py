@@ -44,7 +44,7 @@ def _pinned(t):
 
 
 def run_gpu_host(inp: dict, *, fill: int = 0xA5, stream=None, partial_scale: float = 1.0,
-                 scale_layout: int = 0) -> dict:
+                 scale_layout: int = 0, config: dict | None = None) -> dict:
     """Run the zero-copy entry point on pinned host copies of ``inp`` into guard-banded pinned
     host outputs pre-filled with ``fill``; returns numpy results."""
     T_pad, H, mode = inp["T_pad"], inp["H"], inp["mode"]
@@ -69,14 +69,14 @@ def run_gpu_host(inp: dict, *, fill: int = 0xA5, stream=None, partial_scale: flo
     res_out = _view(res_m, (T_pad, H), torch.bfloat16)
     scale_t = (torch.tensor([inp["scale"]], dtype=torch.float32).pin_memory()
                if inp["scale"] is not None else None)
-    if partial_scale == 1.0 and hin["addend"] is None and scale_layout == 0:
+    if partial_scale == 1.0 and hin["addend"] is None and scale_layout == 0 and config is None:
         sp.sp_fused_reduce_norm_host(hin["partials"], hin["weight"], out, res_out,
                                      residual=hin["residual"], bias=hin["bias"], eps=inp["eps"],
                                      quant_mode=mode, scale=scale_t, out_scales=sc,
                                      T_valid=inp["T_valid"], stream=stream)
     else:
         opts = sp.sp_options_init(partial_scale=partial_scale, addend=hin["addend"],
-                                  scale_layout=scale_layout, host_buffers=True)
+                                  scale_layout=scale_layout, host_buffers=True, launch=config)
         sp.sp_fused_reduce_norm_ex(opts, hin["partials"], hin["weight"], out, res_out,
                                    residual=hin["residual"], bias=hin["bias"], eps=inp["eps"],
                                    quant_mode=mode, scale=scale_t, out_scales=sc,

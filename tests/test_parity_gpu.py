@@ -675,6 +675,20 @@ def test_split_rows_with_options(mode, split):
     compare(a, run_oracle(inp, partial_scale=0.5, scale_layout=layout), inp)
 
 
+@pytest.mark.parametrize("mode", ["fp8_per_token", "nvfp4"])
+def test_split_rows_on_host_buffers(mode):
+    """A forced split-row launch on page-locked host buffers (zero-copy), NVFP4 with the
+    swizzled scale layout."""
+    w = dict(synth.workload(3), mode=mode, scale=None)
+    inp = synth.make_inputs(w, device=DEV, tp=8, T_pad=16, T_valid=13, H=4096)
+    layout = 1 if mode == "nvfp4" else 0
+    a = run_gpu_host(inp, fill=0xA5, scale_layout=layout, config=_split_cfg(8, 1))
+    b = run_gpu_host(inp, fill=0x5A, scale_layout=layout, config=_split_cfg(8, 1))
+    for k in ("out", "out_scales", "residual_out"):
+        assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+    compare(a, run_oracle(inp, scale_layout=layout), inp)
+
+
 def test_split_rows_captured_in_a_graph_after_other_kernels():
     """Split-row launches (clusters with the programmatic-dependent-launch attribute) inside a
     CUDA graph, each after a PyTorch kernel that rewrites its partials: every replay computes on
