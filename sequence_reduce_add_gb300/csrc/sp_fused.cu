@@ -329,10 +329,10 @@ cudaError_t set_staged_smem_limit(DeviceInfo* dev) {
 
 // Split rows: clusters of `split` CTAs (one row each at a time), as many as the SMs hold at the
 // requested CTAs per SM, and never more than rows; launched with PDL like the rest.
-template <int kVec, int kMode, int kSplit>
+template <int kVec, int kMode, int kSplit, int kBatch>
 cudaError_t launch_split(const sp_launch_config& cfg, const spk::Params& p, cudaStream_t stream,
                          DeviceInfo* dev) {
-  auto kernel = spk::k_direct<kVec, kMode, kSplit>;
+  auto kernel = spk::k_direct<kVec, kMode, kSplit, kBatch>;
   int resident = 0;
   cudaError_t e = resident_ctas(kernel, p.nthreads, 0, dev->id, &resident);
   if (e != cudaSuccess) return e;
@@ -359,6 +359,42 @@ cudaError_t launch_split(const sp_launch_config& cfg, const spk::Params& p, cuda
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+template <int kVec, int kMode, int kSplit, int kBatch>
+cudaError_t launch_direct(const sp_launch_config& cfg, spk::Params& p, cudaStream_t stream,
+                          DeviceInfo* dev) {
+  if constexpr (kSplit > 1) {
+    return launch_split<kVec, kMode, kSplit, kBatch>(cfg, p, stream, dev);
+  } else {
+    auto kernel = spk::k_direct<kVec, kMode, 1, kBatch>;
+    int grid = 0;
+    cudaError_t e = persistent_grid(kernel, p.nthreads, 0, cfg.ctas_per_sm, p.T_pad, dev, &grid);
+    if (e != cudaSuccess) return e;
+    e = launch_pdl(kernel, grid, p.nthreads, 0, stream, p);
+    return e != cudaSuccess ? e : cudaGetLastError();
+  }
+}
+
+// One vector per thread and more than four partials: eight partial rows in flight at a time when
+// every CTA the call needs is resident at once (that variant takes about twice the registers, so
+// fewer CTAs fit per SM), else four.
+template <int kVec, int kMode, int kSplit>
+cudaError_t launch_direct_batched(const sp_launch_config& cfg, spk::Params& p,
+                                  cudaStream_t stream, DeviceInfo* dev) {
+  if constexpr (kVec == 1) {
+    if (p.tp > 4) {
+      int resident = 0;
+      const cudaError_t e =
+          resident_ctas(spk::k_direct<kVec, kMode, kSplit, 8>, p.nthreads, 0, dev->id, &resident);
+      if (e != cudaSuccess) return e;
+      const int per_sm = cfg.ctas_per_sm < resident ? cfg.ctas_per_sm : resident;
+      const int64_t slots = static_cast<int64_t>(dev->sms.load(std::memory_order_relaxed)) * per_sm;
+      if (p.rows_total * kSplit <= slots)
+        return launch_direct<kVec, kMode, kSplit, 8>(cfg, p, stream, dev);
+    }
+  }
+  return launch_direct<kVec, kMode, kSplit, 4>(cfg, p, stream, dev);
+}
+
 template <int kVec, int kMode>
 cudaError_t launch_one(const sp_launch_config& cfg, spk::Params& p, int smem, int schedule,
                        cudaStream_t stream, DeviceInfo* dev) {
@@ -366,17 +402,13 @@ cudaError_t launch_one(const sp_launch_config& cfg, spk::Params& p, int smem, in
   if (cfg.kernel == SP_KERNEL_DIRECT) {
     if constexpr (kVec <= 2) {
       switch (split_of(cfg)) {
-        case 2: return launch_split<kVec, kMode, 2>(cfg, p, stream, dev);
-        case 4: return launch_split<kVec, kMode, 4>(cfg, p, stream, dev);
-        case 8: return launch_split<kVec, kMode, 8>(cfg, p, stream, dev);
+        case 2: return launch_direct_batched<kVec, kMode, 2>(cfg, p, stream, dev);
+        case 4: return launch_direct_batched<kVec, kMode, 4>(cfg, p, stream, dev);
+        case 8: return launch_direct_batched<kVec, kMode, 8>(cfg, p, stream, dev);
         default: break;
       }
     }
-    auto kernel = spk::k_direct<kVec, kMode, 1>;
-    cudaError_t e = persistent_grid(kernel, p.nthreads, 0, cfg.ctas_per_sm, p.T_pad, dev, &grid);
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(kernel, grid, p.nthreads, 0, stream, p);
-    return e != cudaSuccess ? e : cudaGetLastError();
+    return launch_direct_batched<kVec, kMode, 1>(cfg, p, stream, dev);
   }
   const int threads = p.nthreads + spk::kProducerThreads;
   cudaError_t e = set_staged_smem_limit<kVec, kMode, false>(dev);

@@ -278,8 +278,12 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
 // vectors [r * split_chunk, (r + 1) * split_chunk) of it; the CTAs combine the row's sum of
 // squares (and max) through distributed shared memory. A call with few rows then draws on
 // kSplit times as many SMs.
-template <int kVec, int kMode, int kSplit>
+// kBatch: partial rows whose loads are in flight together (4, or 8 with one vector per thread:
+// more in flight per row, about twice the registers).
+template <int kVec, int kMode, int kSplit, int kBatch>
 __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) {
+  static_assert(kBatch == 4 || (kBatch == 8 && kVec == 1), "batch of 4, or 8 at one vector");
+  constexpr bool kEarlyResidual = kVec <= 2;  // residual row loaded before the partials
   __shared__ RedSlot slots[64];
   __shared__ float2 cslots[2];
   const int c = threadIdx.x;
@@ -307,27 +311,58 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
 #pragma unroll
       for (int e = 0; e < 8; ++e) h[k][e] = 0.0f;
 
+    // The residual row's loads go out first, then the partials' kBatch rows at a time (every
+    // batch full width, the missing rows predicated off), so a row costs about one round trip to
+    // memory per batch.
+    uint4 xres[kVec];
+#pragma unroll
+    for (int k = 0; k < kVec; ++k) {
+      const int v = vc + k * nc;
+      xres[k] = (kEarlyResidual && p.residual && v < vend) ? ldg_stream(p.residual + t * H + v * 8)
+                                                           : make_uint4(0, 0, 0, 0);
+    }
     const uint16_t* row = p.partials + t * H;
     int r = 0;
-    for (; r + 4 <= p.tp; r += 4) {
-      uint4 x[4][kVec];
+    if constexpr (kVec <= 2) {
+#pragma unroll 1
+      for (; r < p.tp; r += kBatch) {
+        uint4 x[kBatch][kVec];
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
+        for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+          for (int k = 0; k < kVec; ++k) {
+            const int v = vc + k * nc;
+            x[u][k] = (r + u < p.tp && v < vend) ? ldg_stream(row + (r + u) * p.plane + v * 8)
+                                                 : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+          if (r + u < p.tp) {
+#pragma unroll
+            for (int k = 0; k < kVec; ++k) add_bf16x8(x[u][k], h[k]);
+          }
+      }
+    } else {  // four vectors per thread: full batches, then the rest one row at a time
+      for (; r + kBatch <= p.tp; r += kBatch) {
+        uint4 x[kBatch][kVec];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+          for (int k = 0; k < kVec; ++k) {
+            const int v = vc + k * nc;
+            x[u][k] = v < vend ? ldg_stream(row + (r + u) * p.plane + v * 8) : make_uint4(0, 0, 0, 0);
+          }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u)
+#pragma unroll
+          for (int k = 0; k < kVec; ++k) add_bf16x8(x[u][k], h[k]);
+      }
+      for (; r < p.tp; ++r) {
 #pragma unroll
         for (int k = 0; k < kVec; ++k) {
           const int v = vc + k * nc;
-          x[u][k] = v < vend ? ldg_stream(row + (r + u) * p.plane + v * 8) : make_uint4(0, 0, 0, 0);
+          if (v < vend) add_bf16x8(ldg_stream(row + r * p.plane + v * 8), h[k]);
         }
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-#pragma unroll
-        for (int k = 0; k < kVec; ++k) add_bf16x8(x[u][k], h[k]);
-    }
-    for (; r < p.tp; ++r) {
-#pragma unroll
-      for (int k = 0; k < kVec; ++k) {
-        const int v = vc + k * nc;
-        if (v < vend) add_bf16x8(ldg_stream(row + r * p.plane + v * 8), h[k]);
       }
     }
     if (p.partial_scale != 1.0f) {
@@ -338,7 +373,10 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
 #pragma unroll
       for (int k = 0; k < kVec; ++k) {
         const int v = vc + k * nc;
-        if (v < vend) add_bf16x8(ldg_stream(p.residual + t * H + v * 8), h[k]);
+        if (kEarlyResidual)
+          add_bf16x8(xres[k], h[k]);
+        else if (v < vend)
+          add_bf16x8(ldg_stream(p.residual + t * H + v * 8), h[k]);
       }
     }
     if (p.addend) {
