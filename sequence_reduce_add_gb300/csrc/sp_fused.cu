@@ -591,15 +591,17 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   //                        and T <= 256, 13-70 % faster than the deep ring);
   //   4096 < H <= 8192:    split rows (one vector per thread) for few rows: tp >= 12, 8 CTAs
   //                        per row up to 16 rows and 4 up to 64 (10-100 % faster); 6 <= tp < 12,
-  //                        8 up to 8 rows and 4 up to 32 (5-32 %); tp 2-5 at H >= 7168, 8 up to
-  //                        8 rows (0-10 %); split rows lost at H <= 4096. Otherwise direct while
-  //                        tp * T * H <= 2^20 (13-30 % faster at T = 8-64); for 64-128 rows, the
-  //                        staged kernel at one CTA per SM with every stage that fits (a 12-stage
-  //                        ring at H = 8192: 10-34 % faster);
-  //   H > 8192:            split rows, 8 CTAs per row, one vector per thread: up to 64 rows for
-  //                        tp >= 12, 32 for 6 <= tp < 12, 16 for tp 2-5 (2-85 % faster); else
-  //                        direct (four vectors per thread) up to 32 rows (7-35 % faster than
-  //                        the staged kernel; at 64 rows it was 3-11 % slower);
+  //                        8 up to 8 rows, 4 up to 32 and 2 up to 64 (5-35 %); tp 2-5 at
+  //                        H >= 7168, 8 up to 8 rows (0-10 %); split rows lost at H <= 4096.
+  //                        Otherwise direct while tp * T * H <= 2^20 (13-30 % faster at T = 8-64)
+  //                        or, for tp >= 12, up to 128 rows (0-29 %); for 64-128 rows, the staged
+  //                        kernel at one CTA per SM with every stage that fits (a 12-stage ring
+  //                        at H = 8192: 10-34 % faster);
+  //   H > 8192:            split rows, one vector per thread: 8 CTAs per row up to 64 rows for
+  //                        tp >= 12; 8 up to 32 and 4 up to 64 for 6 <= tp < 12; 8 up to 16 and
+  //                        (tp >= 3) 4 up to 32 for tp 2-5 (2-85 % faster); else direct (four
+  //                        vectors per thread) up to 32 rows (7-35 % faster than the staged
+  //                        kernel; at 64 rows it was 3-11 % slower);
   //   4096 < H <= 6144, more rows than SMs but no more than one round of the large-call grid:
   //                        ceil(T / SMs) CTAs per SM, every stage that fits (6-27 % faster at
   //                        T = 160-456; at H = 4096 and from 7168 up it was a wash);
@@ -622,18 +624,18 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     if (tp >= 12)
       split = T_pad <= 16 ? 8 : (T_pad <= 64 ? 4 : 0);
     else if (tp >= 6)
-      split = T_pad <= 8 ? 8 : (T_pad <= 32 ? 4 : 0);
+      split = T_pad <= 8 ? 8 : (T_pad <= 32 ? 4 : (T_pad <= 64 ? 2 : 0));
     else if (tp >= 2 && H >= 7168)
       split = T_pad <= 8 ? 8 : 0;
-    direct = split > 0 || elems <= (int64_t{1} << 20);
+    direct = split > 0 || elems <= (int64_t{1} << 20) || (tp >= 12 && T_pad <= 128);
     deep_ring_1 = !direct && T_pad >= 64 && T_pad <= 128;
   } else {
     if (tp >= 12)
       split = T_pad <= 64 ? 8 : 0;
     else if (tp >= 6)
-      split = T_pad <= 32 ? 8 : 0;
+      split = T_pad <= 32 ? 8 : (T_pad <= 64 ? 4 : 0);
     else if (tp >= 2)
-      split = T_pad <= 16 ? 8 : 0;
+      split = T_pad <= 16 ? 8 : (tp >= 3 && T_pad <= 32 ? 4 : 0);
     direct = split > 0 || T_pad <= 32;
   }
   if (direct) {

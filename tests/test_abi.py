@@ -114,10 +114,12 @@ def test_launch_selection(lib):
     # split rows: a cluster of 8 or 4 CTAs per row, one vector per thread
     (8, 8, 8192, (1, 1, 8, 0, 8)),
     (8, 32, 5120, (1, 1, 8, 0, 4)),
-    (8, 40, 5120, (0, 2, 3, 4)),        # more rows: no split
+    (8, 40, 5120, (1, 1, 8, 0, 2)),     # 33-64 rows at 6 <= tp < 12: 2 CTAs per row
+    (8, 72, 5120, (0, 2, 1, 0)),        # more rows: no split
     (16, 16, 7168, (1, 1, 8, 0, 8)),
     (16, 64, 8192, (1, 1, 8, 0, 4)),
-    (16, 80, 8192, (0, 2, 1, 0)),
+    (16, 80, 8192, (1, 2, 8, 0)),       # tp >= 12: direct up to 128 rows
+    (16, 144, 8192, (0, 2, 2, 4)),
     (2, 8, 7168, (1, 1, 8, 0, 8)),
     (4, 8, 5120, (1, 2, 8, 0)),         # tp < 6 splits only from H = 7168
     (4, 16, 8192, (1, 2, 8, 0)),
@@ -126,14 +128,16 @@ def test_launch_selection(lib):
     # H > 8192: split rows, else direct with four vectors per thread, for few rows
     (2, 16, 16384, (1, 1, 8, 0, 8)),
     (2, 32, 16384, (1, 4, 8, 0)),
-    (4, 32, 12288, (1, 4, 8, 0)),
+    (4, 32, 12288, (1, 1, 8, 0, 4)),
+    (2, 32, 12288, (1, 4, 8, 0)),
     (4, 64, 12288, (0, 4, 1, 4)),
     (8, 32, 12288, (1, 1, 8, 0, 8)),
-    (8, 64, 16384, (0, 4, 1, 4)),
+    (8, 64, 16384, (1, 1, 8, 0, 4)),
+    (8, 72, 16384, (0, 4, 1, 4)),
     (16, 64, 16384, (1, 1, 8, 0, 8)),
     (16, 128, 16384, (0, 4, 1, 4)),
-    (8, 64, 8192, (0, 2, 1, 0)),        # 64-128 rows: one CTA per SM, deepest ring
-    (16, 128, 7168, (0, 2, 1, 0)),
+    (8, 72, 8192, (0, 2, 1, 0)),        # 64-128 rows: one CTA per SM, deepest ring
+    (4, 128, 7168, (0, 2, 1, 0)),
     (16, 256, 7168, (0, 2, 2, 4)),
     (8, 256, 5120, (0, 2, 2, 0)),       # one round of rows at H = 5120: 2 CTAs/SM, deep ring
     (8, 384, 5120, (0, 2, 3, 0)),

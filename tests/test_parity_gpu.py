@@ -605,6 +605,8 @@ def test_dynamic_schedule_soak_two_chained_streams():
     (16, 128, 2048, "fp8_static", (1, 1, 16, 0)),     # direct at tp >= 6
     (16, 16, 8192, "fp8_per_token", (1, 1, 8, 0, 8)), # split rows, 8 CTAs per row
     (8, 32, 5120, "nvfp4", (1, 1, 8, 0, 4)),          # split rows, 4 CTAs per row
+    (8, 48, 7168, "fp8_per_token", (1, 1, 8, 0, 2)),  # split rows, 2 CTAs per row
+    (16, 96, 5120, "nvfp4", (1, 2, 8, 0)),            # direct up to 128 rows at tp >= 12
     (2, 24, 16384, "fp8_static", (1, 4, 8, 0)),       # direct, four vectors per thread
     (16, 48, 12288, "nvfp4", (1, 1, 8, 0, 8)),        # split rows at H > 8192
     (8, 96, 7168, "nvfp4", (0, 2, 1, 0)),             # staged, one CTA per SM
