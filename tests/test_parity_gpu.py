@@ -651,6 +651,18 @@ def test_split_rows_longest_hidden(mode, split, vec):
     assert _check(inp, config=_split_cfg(split, vec))
 
 
+@pytest.mark.parametrize("T,split", [(64, 0), (2048, 0), (48, 4), (4096, 2)])
+@pytest.mark.parametrize("tp", [5, 8, 13])
+def test_direct_kernel_batches_of_partials(tp, T, split):
+    """One vector per thread with more than four partials: the variant with eight partial rows in
+    flight (few rows, every CTA resident) and the one with four (more rows than fit at once),
+    including a last batch that is only partly filled."""
+    w = dict(synth.workload(4), tp=tp)
+    inp = synth.make_inputs(w, device=DEV, tp=tp, T_pad=tp * -(-T // tp), T_valid=T - 5, H=2048)
+    cfg = dict(kernel=1, vec_per_thread=1, ctas_per_sm=16, stages=0, split=split)
+    assert _check(inp, config=cfg)
+
+
 @pytest.mark.parametrize("split,ctas", [(8, 1), (4, 1), (2, 1)])
 def test_split_rows_many_rows_per_cluster(split, ctas):
     """Fewer clusters than rows: each cluster takes several rows in turn, reusing its two
