@@ -1,5 +1,6 @@
 // sp_kernels.cuh — the two kernels of the fused stage. Both map one token row at a time to one
-// CTA (rows are independent: RMSNorm and every scale kind used here are per token), walk rows
+// CTA, or to one cluster of CTAs in k_direct's split variant (rows are independent: RMSNorm and
+// every scale kind used here are per token), walk rows
 // in token order (a grid stride, or claimed in the staged kernel's dynamic variant below), and
 // make a single pass over HBM: every partial, residual and output byte of a valid row is read
 // or written exactly once; padding rows are written as zeros without any read.
@@ -19,7 +20,9 @@
 //             all finish within about one row of each other. The producer passes each row's index
 //             to the consumers beside the row's first ring stage.
 //   k_direct  The consumer threads load their vectors of every segment straight into registers
-//             with 128-bit non-coherent loads, four partials at a time.
+//             with 128-bit non-coherent loads: the residual row first, then the partials four or
+//             eight rows at a time. Its split variant shares each row among the CTAs of a
+//             thread-block cluster, each owning a contiguous slice, for calls with few rows.
 #pragma once
 
 #include "sp_device.cuh"
