@@ -576,9 +576,10 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     c.stages = 0;
   }
   // Small calls (decode-sized batches) are latency-bound, every CTA doing about one row. The
-  // direct kernel (no ring to set up; loads four partials at a time) is fastest while its loads
-  // fit in one wave; the staged kernel's floor grows with the row's segment count (each passes
-  // through the ring in turn), but it keeps all of a row's segments in flight with a deep ring.
+  // direct kernel (no ring to set up; loads four or eight partials at a time) is fastest while
+  // its loads fit in one wave; the staged kernel's floor grows with the row's segment count
+  // (each passes through the ring in turn), but it keeps all of a row's segments in flight with a
+  // deep ring.
   // With only a few rows, one SM per row caps the call at what an SM can pull in (about
   // 45 GB/s): splitting each row across a cluster of 4 or 8 CTAs draws on that many more SMs.
   // From GB300 sweeps of tp 2-16, H 1024-16384, T 1-4096 (call time, launches replayed from a
