@@ -703,6 +703,32 @@ def test_split_rows_on_host_buffers(mode):
     compare(a, run_oracle(inp, scale_layout=layout), inp)
 
 
+def test_split_rows_on_two_streams_concurrently():
+    """Split-row launches (clusters of 8 and of 2 CTAs) on two streams at once, on different
+    buffers, each give their own correct result."""
+    w = synth.workload(4)
+    a = synth.make_inputs(w, device=DEV, tp=16, T_pad=16, T_valid=14, H=8192)
+    b = synth.make_inputs(w, device=DEV, tp=16, T_pad=64, T_valid=61, H=8192, seed=a["seed"] + 3)
+    oa = sp.allocate_outputs(a["T_pad"], a["H"], a["mode"], DEV)
+    ob = sp.allocate_outputs(b["T_pad"], b["H"], b["mode"], DEV)
+    sa, sb = torch.cuda.Stream(device=DEV), torch.cuda.Stream(device=DEV)
+
+    def call(inp, outs, cfg, stream):
+        sp.sp_fused_reduce_norm_ex(sp.sp_options_init(launch=cfg), inp["partials"], inp["weight"],
+                                   outs["out"], outs["residual_out"], residual=inp["residual"],
+                                   bias=inp["bias"], eps=inp["eps"], quant_mode=inp["mode"],
+                                   out_scales=outs["out_scales"], T_valid=inp["T_valid"],
+                                   stream=stream)
+
+    torch.cuda.synchronize()
+    for _ in range(20):
+        call(a, oa, _split_cfg(8, 1), sa)
+        call(b, ob, _split_cfg(2, 1), sb)
+    torch.cuda.synchronize()
+    compare(_host(oa), run_oracle(a), a)
+    compare(_host(ob), run_oracle(b), b)
+
+
 def test_split_rows_captured_in_a_graph_after_other_kernels():
     """Split-row launches (clusters with the programmatic-dependent-launch attribute) inside a
     CUDA graph, each after a PyTorch kernel that rewrites its partials: every replay computes on
