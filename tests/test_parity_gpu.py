@@ -651,6 +651,24 @@ def test_split_rows_longest_hidden(mode, split, vec):
     assert _check(inp, config=_split_cfg(split, vec))
 
 
+@pytest.mark.parametrize("mode", ["fp8_per_token", "nvfp4"])
+@pytest.mark.parametrize("tp,T_pad,T_valid,layout", [(1, 8, 8, 0), (4, 16, 0, 0), (4, 16, 0, 1),
+                                                     (1, 1, 1, 1), (2, 130, 127, 1)])
+def test_split_rows_edge_cases(mode, tp, T_pad, T_valid, layout):
+    """Split rows at tp = 1, with every row padding (only zeros written, scales included), with
+    a single row, and with the swizzled layout's padding rows beyond T_pad (NVFP4)."""
+    if layout and mode != "nvfp4":
+        pytest.skip("the swizzled layout is NVFP4-only")
+    w = dict(synth.workload(3), mode=mode, scale=None)
+    inp = synth.make_inputs(w, device=DEV, tp=tp, T_pad=T_pad, T_valid=T_valid, H=2080)
+    kw = dict(config=_split_cfg(8, 1), scale_layout=layout)
+    a = run_gpu(inp, fill=0xA5, **kw)
+    b = run_gpu(inp, fill=0x5A, **kw)
+    for k in ("out", "out_scales", "residual_out"):
+        assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+    compare(a, run_oracle(inp, scale_layout=layout), inp)
+
+
 @pytest.mark.parametrize("T,split", [(64, 0), (2048, 0), (48, 4), (4096, 2)])
 @pytest.mark.parametrize("tp", [5, 8, 13])
 def test_direct_kernel_batches_of_partials(tp, T, split):
