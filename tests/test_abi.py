@@ -352,3 +352,30 @@ def test_fc2_argument_checks(lib, kw, want):
     st = sp.sp_fc2_check_args(a["x"], a["global_tp"], a["otp_size"], a["N"], a["H"],
                               a["elem_bytes"], a["y"])
     assert sp.sp_status_string(st) == want
+
+
+def test_every_selected_launch_passes_the_launch_checks(lib):
+    """Over a grid of tp, H, T and modes, the configuration sp_select_launch picks passes the
+    checks a forced configuration gets (kernel, vector count, threads, ring depth, split), so the
+    default path never picks a launch the library would refuse."""
+    G = 1 << 40  # fake, far-apart 16-byte-aligned addresses: compared, never dereferenced
+    checked = 0
+    for mode in ("none", "fp8_static", "fp8_per_token", "nvfp4"):
+        for tp in (1, 2, 3, 4, 5, 6, 8, 12, 16, 24, 32):
+            for H in (8, 16, 24, 512, 1000, 1024, 2048, 2056, 4096, 5120, 7168, 8192, 12288,
+                      16376, 16384):
+                if mode == "nvfp4" and H % 16:
+                    continue
+                for T in (1, 2, 7, 8, 16, 33, 64, 100, 128, 152, 256, 304, 500, 1024, 4096, 9999):
+                    T_pad = sp.sp_pad_tokens(T, tp)
+                    cfg = sp.sp_select_launch(tp, T_pad, H, mode)
+                    o = sp.Options()
+                    lib.sp_options_init(ctypes.byref(o))
+                    o.launch = ctypes.pointer(cfg)
+                    st = sp.sp_check_args_ex(o, G, tp, T_pad, T, H, 2 * G, 3 * G, 4 * G, 1e-6, mode,
+                                             5 * G if mode in ("fp8_static", "nvfp4") else None,
+                                             6 * G, 7 * G if mode in ("fp8_per_token", "nvfp4") else None,
+                                             8 * G)
+                    assert sp.sp_status_string(st) == "SP_OK", (mode, tp, H, T, cfg.as_dict())
+                    checked += 1
+    assert checked > 9000
