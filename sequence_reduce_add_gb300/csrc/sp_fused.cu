@@ -581,7 +581,7 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   // (each passes through the ring in turn), but it keeps all of a row's segments in flight with a
   // deep ring.
   // With only a few rows, one SM per row caps the call at what an SM can pull in (about
-  // 45 GB/s): splitting each row across a cluster of 4 or 8 CTAs draws on that many more SMs.
+  // 45 GB/s): splitting each row across a cluster of 2, 4 or 8 CTAs draws on that many more SMs.
   // From GB300 sweeps of tp 2-16, H 1024-16384, T 1-4096 (call time, launches replayed from a
   // CUDA graph and single launches):
   //   H <= 4096, tp <= 5, T <= 256: direct below ~1.5M partial elements for tp <= 4 (2M for
