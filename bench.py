@@ -541,7 +541,8 @@ def bench_extra(lib, sp, synth, w, device, stream, peak, variant: str | None = N
            "mtokens_per_s": round(w["T_valid"] / (k / 1e3) / 1e6, 3), "kernel_us": round(k * 1e3, 2),
            "isolated_launch_us": round(float(np.mean(launches)) * 1e3, 2), "steps": steps,
            "bytes": one, "cuda_graph_us_per_launch": graph_us,
-           "sets": len(problems)}
+           "sets": len(problems),
+           "launch": sp.sp_select_launch(w["tp"], w["T_pad"], w["H"], w["mode"]).as_dict()}
     del problems
     torch.cuda.empty_cache()
     return res
