@@ -5,9 +5,11 @@
 
 A step is one call of the whole per-token stage (sum of tp partials, bias + residual add, new
 residual, RMSNorm, output in the workload's form, padding rows zeroed) over one batch of
-synthetic, seeded input already resident in HBM. The default workload is tp=4, 4093 tokens padded
-to 4096, H=4096, bf16 output. The timed loop rotates over several input/output sets whose total
-size is far above the 129 MB L2, so every step reads its inputs from HBM.
+synthetic, seeded input already resident in HBM. The default workload is the largest one: tp=8,
+16384 tokens, H=5120, Student-t partials, NVFP4 output (1.72 GB moved per step). Every step's
+inputs are larger than the 129 MB L2, and the timed loop also rotates over resident sets, so every
+step reads its inputs from HBM. The timed launches are queued behind a short GPU-side sleep placed
+before the start event, so the GPU never waits on the Python loop inside the timed region.
 
 Printed: one JSON line (rank 0) with the headline HBM GB/s (algorithmic bytes / time), Mtokens/s,
 the roofline of the kernel against the measured HBM copy peak, the end-to-end figure through the
@@ -39,7 +41,7 @@ import numpy as np  # noqa: E402
 import torch  # noqa: E402
 
 METRIC = "fused reduce+add-RMSNorm+quant HBM GB/s and Mtokens/s; % of GB300 HBM peak"
-DEFAULT_WORKLOAD = "tp4_T4093p4096_H4096_bf16"
+DEFAULT_WORKLOAD = "tp8_T16384_H5120_nvfp4"
 FALLBACK_HBM_GBS = 6800.0
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (for context; `peak` is the measured copy)
 L2_BYTES = 129 * 1024 * 1024
@@ -56,6 +58,15 @@ def algorithmic_bytes(tp: int, T_valid: int, T_pad: int, H: int, mode: str,
     read_row = 2 * H * (tp + (1 if residual else 0) + (1 if addend else 0))
     write_row = 2 * H + out_row
     return T_valid * (read_row + write_row) + (T_pad - T_valid) * write_row
+
+
+def workload_config(w: dict, world: int) -> dict:
+    """The `config` object of the JSON line; identical in both arms for the same workload."""
+    one = algorithmic_bytes(w["tp"], w["T_valid"], w["T_pad"], w["H"], w["mode"])
+    return {"workload": w["name"], "tp": w["tp"], "T_valid": w["T_valid"], "T_pad": w["T_pad"],
+            "H": w["H"], "quant": w["mode"], "bytes_per_step": one,
+            "l2": f"inputs larger than L2 ({one / 1e6:.0f} MB per step, L2 129 MB)",
+            "parallelism": f"replicas x{world}"}
 
 
 KERNEL_SOURCES = ("sp_device.cuh", "sp_kernels.cuh")  # the device code of every kernel
@@ -208,14 +219,38 @@ class Problem:
         return sum(t.numel() * t.element_size() for t in ts if t is not None)
 
 
-def time_kernel_loop(lib, problems, steps: int, stream, per_launch_events: bool):
-    """Launch `steps` calls rotating over `problems` on `stream`; returns (total_ms, [launch ms])."""
+# Host time to enqueue one call (ctypes + checks + launch) is a few microseconds; the gate that
+# holds the GPU while the timed launches are queued is sized from this, generously.
+ENQUEUE_US_PER_CALL = 10.0
+GATE_MAX_LAUNCHES = 1024
+SLEEP_CYCLES_PER_US = 2100  # at most ~2.1 GHz SM clock: a sleep of n cycles lasts >= n/2100 us
+
+
+def gate_stream(stream, launches: int) -> None:
+    """Hold `stream` in a short device-side sleep long enough for the host to enqueue `launches`
+    calls behind it (at most GATE_MAX_LAUNCHES), so the timed launches start back to back instead
+    of waiting for the Python loop. The sleep runs before the start event: it is not timed."""
+    us = 100.0 + ENQUEUE_US_PER_CALL * min(launches, GATE_MAX_LAUNCHES)
+    with torch.cuda.stream(stream):
+        torch.cuda._sleep(int(us * SLEEP_CYCLES_PER_US))
+
+
+def time_kernel_loop(lib, problems, steps: int, stream, per_launch_events: bool,
+                     gate: bool = False, end_events: bool = False):
+    """Launch `steps` calls rotating over `problems` on `stream`; returns (total_ms, [launch ms],
+    info). per_launch_events: an event pair around every launch (isolated launches). end_events:
+    one event after every launch (consecutive differences = per-launch times in a chain). gate:
+    queue everything behind gate_stream; info["host_ahead"] says whether the host had queued every
+    launch before the GPU reached the start event."""
     handle = ctypes.c_void_p(stream.cuda_stream)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     ev = ([(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            for _ in range(steps)] if per_launch_events else None)
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)] if end_events else None
     fn = getattr(lib, problems[0].fn_name)
     n = len(problems)
+    if gate:
+        gate_stream(stream, steps)
     start.record(stream)
     for s in range(steps):
         if ev:
@@ -225,11 +260,17 @@ def time_kernel_loop(lib, problems, steps: int, stream, per_launch_events: bool)
             raise RuntimeError(f"{problems[0].fn_name} returned {st}")
         if ev:
             ev[s][1].record(stream)
+        if ends:
+            ends[s].record(stream)
     end.record(stream)
+    host_ahead = not start.query() if gate else None
     torch.cuda.synchronize()
     total = start.elapsed_time(end)
     launches = [a.elapsed_time(b) for a, b in ev] if ev else []
-    return total, launches
+    if ends:
+        marks = [start] + ends
+        launches = [a.elapsed_time(b) for a, b in zip(marks[:-1], marks[1:])]
+    return total, launches, {"host_ahead": host_ahead}
 
 
 def e2e_loop(sp, w: dict, problem: Problem, steps: int, warmup: int, stream) -> dict:
@@ -407,16 +448,18 @@ def run_ours(args) -> None:
     rotation_bytes = sum(p.nbytes() for p in problems)
     stream = torch.cuda.Stream(device=device)
 
-    # warm-up, then the timed region (barrier + synchronize on both sides)
-    time_kernel_loop(lib, problems, max(args.warmup, 3), stream, False)
-    if dist:
-        dist.barrier()
-    torch.cuda.synchronize()
+    # The clock sampler starts first, so that the GPU does not idle between the warm-up and the
+    # timed region; then warm-up, then the timed region (barrier + synchronize on both sides).
+    # The timed launches are queued behind a device-side sleep that ends before the start event.
     with ClockSampler(local) as clocks:
+        time_kernel_loop(lib, problems, max(args.warmup, 3), stream, False)
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
         t0 = time.time()
-        total_ms, _ = time_kernel_loop(lib, problems, args.steps, stream, False)
+        total_ms, _, info = time_kernel_loop(lib, problems, args.steps, stream, False, gate=True)
         t1 = time.time()
-    torch.cuda.synchronize()
+        torch.cuda.synchronize()
     if dist:
         dist.barrier()
         total_ms = max_over_ranks(total_ms, device)
@@ -425,10 +468,14 @@ def run_ours(args) -> None:
     mtok = w["T_valid"] * args.steps * world / (total_ms / 1e3) / 1e6
     # The timed loop is one kernel per step launched back to back (consecutive launches overlap
     # their launch latency and prologue through programmatic dependent launch), so the kernel's
-    # average launch duration is the timed region over the launches. An event-bracketed launch
-    # (no overlap with its neighbours) is reported beside it.
+    # average launch duration is the timed region over the launches. Beside it: the same chain
+    # with an event after every launch (per-launch times of the first launches, to show the
+    # timed region is steady from its start), and event-bracketed launches (no overlap with
+    # their neighbours).
     kernel_ms = ms_per_step
-    _, isolated = time_kernel_loop(lib, problems, min(args.steps, 300), stream, True)
+    _, chain, _ = time_kernel_loop(lib, problems, min(args.steps, 20), stream, False, gate=True,
+                                   end_events=True)
+    _, isolated, _ = time_kernel_loop(lib, problems, min(args.steps, 300), stream, True)
     isolated_ms = float(np.mean(isolated))
     isolated_median_ms, isolated_min_ms = float(np.median(isolated)), float(np.min(isolated))
     peak, peak_kind = measured_peak()
@@ -467,12 +514,10 @@ def run_ours(args) -> None:
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic (seeded; bf16 inputs as in the workload definition)",
         "mtokens_per_s": round(mtok, 3),
-        "config": {"workload": w["name"], "tp": w["tp"], "T_valid": w["T_valid"],
-                   "T_pad": w["T_pad"], "H": w["H"], "quant": w["mode"],
-                   "bytes_per_step": one, "launch": cfg,
-                   "l2": f"inputs larger than L2: {len(problems)} resident sets rotated, "
-                         f"{rotation_bytes / 1e6:.0f} MB per rotation (L2 129 MB)",
-                   "parallelism": f"replicas x{world}"},
+        "config": workload_config(w, world),
+        "launch": cfg,
+        "rotation": f"{len(problems)} resident input/output sets rotated, "
+                    f"{rotation_bytes / 1e6:.0f} MB per rotation",
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "peak_kind": peak_kind,
                      "traffic": ncu_traffic(w["name"], cfg), "kernel_ms": round(kernel_ms, 6),
@@ -481,8 +526,11 @@ def run_ours(args) -> None:
                      "isolated_launch_ms_min": round(isolated_min_ms, 6),
                      "isolated_frac": round(one / (isolated_ms / 1e3) / 1e9 / peak, 4),
                      "kernel": "k_staged" if cfg["kernel"] == 0 else "k_direct",
+                     "peak_note": "peak = measured HBM copy (torch copy_, read + write bytes)",
                      "nominal_peak": NOMINAL_HBM_GBS,
-                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4)},
+                     "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
+                     "host_ahead": info["host_ahead"],
+                     "chain_launch_us": [round(x * 1e3, 2) for x in chain]},
         "e2e": {"value": round(e2e_value, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": e2e["h2d_bytes_per_step"],
                 "d2h_bytes_per_step": e2e["d2h_bytes_per_step"],
@@ -511,8 +559,8 @@ def bench_extra(lib, sp, synth, w, device, stream, peak, variant: str | None = N
     # about 50 ms of timed launches at ~6.5 TB/s (at least 20, at most 4000 launches)
     steps = int(min(4000, max(20, 0.05 * 6.5e12 / max(one, 1))))
     time_kernel_loop(lib, problems, 10, stream, False)
-    total, _ = time_kernel_loop(lib, problems, steps, stream, False)
-    _, launches = time_kernel_loop(lib, problems, min(steps, 100), stream, True)
+    total, _, _ = time_kernel_loop(lib, problems, steps, stream, False, gate=True)
+    _, launches, _ = time_kernel_loop(lib, problems, min(steps, 100), stream, True)
     k = total / steps
     gbs = one / (k / 1e3) / 1e9
     graph_us = None
@@ -538,6 +586,7 @@ def bench_extra(lib, sp, synth, w, device, stream, peak, variant: str | None = N
         graph_us = round(a.elapsed_time(b) / 2000 * 1e3, 2)
         del g
     res = {"GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+           "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
            "mtokens_per_s": round(w["T_valid"] / (k / 1e3) / 1e6, 3), "kernel_us": round(k * 1e3, 2),
            "isolated_launch_us": round(float(np.mean(launches)) * 1e3, 2), "steps": steps,
            "bytes": one, "cuda_graph_us_per_launch": graph_us,
@@ -549,6 +598,7 @@ def bench_extra(lib, sp, synth, w, device, stream, peak, variant: str | None = N
 
 
 FC2_WORKLOAD = "fc2_reorganize_G8_otp2_N8192_H7168_bf16"
+REFERENCE_ROWS = 4096  # rows of the workload the reference arm draws on the host
 
 
 def run_kernel_only(args) -> None:
@@ -580,7 +630,7 @@ def run_kernel_only(args) -> None:
     stream = torch.cuda.Stream(device=device)
     if args.warmup:
         time_kernel_loop(lib, problems, args.warmup, stream, False)
-    total_ms, launches = time_kernel_loop(lib, problems, args.steps, stream, True)
+    total_ms, launches, _ = time_kernel_loop(lib, problems, args.steps, stream, True)
     one = algorithmic_bytes(w["tp"], w["T_valid"], w["T_pad"], w["H"], w["mode"])
     k = float(np.mean(launches))
     print(json.dumps({"workload": w["name"], "launches": args.steps, "sets": len(problems),
@@ -607,6 +657,7 @@ def bench_fc2(lib, device, stream, peak, G=8, P=2, N=8192, H=7168) -> dict:
         lib.sp_fc2_reorganize(*args[k % sets])
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gate_stream(stream, steps)
     a.record(stream)
     for k in range(steps):
         st = lib.sp_fc2_reorganize(*args[k % sets])
@@ -619,6 +670,7 @@ def bench_fc2(lib, device, stream, peak, G=8, P=2, N=8192, H=7168) -> dict:
     del xs, ys
     torch.cuda.empty_cache()
     return {"GB_per_s": round(gbs, 1), "frac_of_peak": round(gbs / peak, 4),
+            "frac_of_nominal": round(gbs / NOMINAL_HBM_GBS, 4),
             "kernel_us": round(ms * 1e3, 2), "steps": steps, "bytes": one, "sets": sets,
             "mtokens_per_s": round(N / (ms / 1e3) / 1e6, 3)}
 
@@ -636,11 +688,14 @@ def run_reference(args) -> None:
     from sequence_reduce_add_gb300 import synth
     oracle_build.build()
     w = synth.workload(args.workload if not str(args.workload).isdigit() else int(args.workload))
-    inp = synth.make_inputs(w, device="cpu")
+    # The oracle computes a bounded row sample per step, so only the first REFERENCE_ROWS rows of
+    # the workload are drawn (same shape, mode and distributions; a multiple of tp).
+    rows_drawn = min(w["T_pad"], max(w["tp"], REFERENCE_ROWS // w["tp"] * w["tp"]))
+    inp = synth.make_inputs(w, device="cpu", T_pad=rows_drawn)
     host_in = {k: inp[k] for k in ("partials", "residual", "weight", "bias") if inp[k] is not None}
     if inp["scale"] is not None:
         host_in["scale"] = inp["scale"]
-    runner = OracleRunner(w, host_in)
+    runner = OracleRunner(dict(w, T_pad=rows_drawn, T_valid=inp["T_valid"]), host_in)
     total_steps = max(args.warmup, 0) + args.steps
     rows = runner.rows_for(args.reference_budget_s / max(total_steps, 1))
     for _ in range(max(args.warmup, 0)):
@@ -651,20 +706,19 @@ def run_reference(args) -> None:
         secs += dt
         nbytes += b
     value = nbytes / secs / 1e9
-    tok = min(rows, w["T_valid"]) * args.steps
-    one = algorithmic_bytes(w["tp"], w["T_valid"], w["T_pad"], w["H"], w["mode"])
+    rows = min(rows, inp["T_valid"])
+    tok = rows * args.steps
     cpu = {"value": round(value, 4), "unit": "GB/s", "cores": runner.cores, "kind": "oracle",
-           "sample": f"{min(rows, w['T_valid'])} rows of {w['T_valid']} per step, "
-                     f"{args.steps} timed steps, {secs:.1f} s, {runner.cores} threads"}
+           "sample": f"{rows} valid rows per step (of the workload's first {rows_drawn} rows, "
+                     f"drawn as in the workload), {args.steps} timed steps, {secs:.1f} s, "
+                     f"{runner.cores} threads"}
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
         "n_gpus": int(os.environ.get("WORLD_SIZE", "1")), "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(secs / args.steps * 1e3, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic (seeded)", "mtokens_per_s": round(tok / secs / 1e6, 4),
-        "config": {"workload": w["name"], "tp": w["tp"], "T_valid": w["T_valid"],
-                   "T_pad": w["T_pad"], "H": w["H"], "quant": w["mode"], "bytes_per_step": one,
-                   "l2": "host run (no GPU)"},
+        "config": workload_config(w, int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": cpu,
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
