@@ -149,13 +149,79 @@ def _stream_handle(stream) -> int | None:
     return stream if isinstance(stream, int) else stream.cuda_stream
 
 
+def _current_device():
+    """The device the library launches on (torch's current CUDA device)."""
+    import torch
+    return torch.device("cuda", torch.cuda.current_device())
+
+
+# Element types each buffer may have (one byte per code for FP8 / packed FP4 / block scales).
+def _dtypes():
+    import torch
+    byte = [torch.uint8, torch.int8]
+    for name in ("float8_e4m3fn", "float4_e2m1fn_x2"):
+        if hasattr(torch, name):
+            byte.append(getattr(torch, name))
+    return {"bf16": (torch.bfloat16,), "f32": (torch.float32,), "byte": tuple(byte)}
+
+
+def _check_tensor(name: str, t, dtypes, min_bytes: int, device, host: bool) -> None:
+    """Raise ValueError unless `t` is a contiguous tensor of one of `dtypes`, at least
+    `min_bytes` long, on `device` (or, with host=True, page-locked host memory)."""
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name}: expected a torch.Tensor, got {type(t).__name__}")
+    if host and t.device.type == "cpu":
+        if not t.is_pinned():
+            raise ValueError(f"{name}: host tensors must be page-locked (tensor.pin_memory())")
+    elif t.device != device:
+        raise ValueError(f"{name}: expected a tensor on {device}, got {t.device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor")
+    if t.dtype not in dtypes:
+        raise ValueError(f"{name}: dtype {t.dtype} not one of {[str(d) for d in dtypes]}")
+    nbytes = t.numel() * t.element_size()
+    if nbytes < min_bytes:
+        raise ValueError(f"{name}: {nbytes} bytes, the call needs at least {min_bytes}")
+
+
 def _main_args(partials, residual, weight, bias, eps, quant_mode, scale, out, out_scales,
-               residual_out, T_valid):
+               residual_out, T_valid, *, host: bool = False, addend=None, scale_layout: int = 0):
+    """Check every tensor against what the call will read and write, then marshal the C
+    arguments. The library can only check sizes derived from the shape arguments, so a buffer
+    that is too small, non-contiguous, of the wrong type or on another device is refused here,
+    before anything is launched."""
+    import torch
+    dev = _current_device()
+    dt = _dtypes()
+    if not isinstance(partials, torch.Tensor) or partials.dim() != 3:
+        raise ValueError("partials: expected a bf16 tensor [tp, T_pad, H]")
     tp, T_pad, H = partials.shape
+    mode = _mode(quant_mode)
     if T_valid is None:
         T_valid = T_pad
+    _check_tensor("partials", partials, dt["bf16"], 0, dev, host)
+    rows = T_pad * H * 2
+    for name, t, need in (("residual", residual, rows), ("addend", addend, rows),
+                          ("bias", bias, H * 2)):
+        if t is not None:
+            _check_tensor(name, t, dt["bf16"], need, dev, host)
+    _check_tensor("weight", weight, dt["bf16"], H * 2, dev, host)
+    _check_tensor("residual_out", residual_out, dt["bf16"], rows, dev, host)
+    if scale is not None:
+        _check_tensor("scale", scale, dt["f32"], 4, dev, host)
+    if mode in (0, 1, 2, 3):
+        out_bytes = {0: rows, 1: T_pad * H, 2: T_pad * H, 3: T_pad * (H // 2)}[mode]
+        _check_tensor("out", out, dt["bf16"] if mode == 0 else dt["byte"], out_bytes, dev, host)
+        if out_scales is not None and mode in (2, 3):
+            if mode == 2:
+                _check_tensor("out_scales", out_scales, dt["f32"], T_pad * 4, dev, host)
+            else:
+                need = (-(-T_pad // 128) * 128 * (-(-(H // 16) // 4) * 4) if scale_layout == 1
+                        else T_pad * (H // 16))
+                _check_tensor("out_scales", out_scales, dt["byte"], need, dev, host)
     return [_ptr(partials), tp, T_pad, T_valid, H, _ptr(residual), _ptr(weight), _ptr(bias),
-            ctypes.c_float(eps), _mode(quant_mode), _ptr(scale), _ptr(out), _ptr(out_scales),
+            ctypes.c_float(eps), mode, _ptr(scale), _ptr(out), _ptr(out_scales),
             _ptr(residual_out)]
 
 
@@ -185,6 +251,7 @@ def sp_options_init(*, partial_scale: float = 1.0, addend=None, scale_layout: in
     load_library().sp_options_init(ctypes.byref(o))
     o.partial_scale = partial_scale
     o.addend = _ptr(addend)
+    o._addend_ref = addend  # checked (and kept alive) by the call that uses these options
     o.scale_layout = scale_layout
     o.host_buffers = 1 if host_buffers else 0
     o.schedule = SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
@@ -202,7 +269,10 @@ def sp_fused_reduce_norm_ex(options: Options | None, partials, weight, out, resi
     """``sp_fused_reduce_norm`` with options (``sp_options_init``): a scale applied to every
     partial before the reduction, an addend after it, host buffers."""
     args = _main_args(partials, residual, weight, bias, eps, quant_mode, scale, out, out_scales,
-                      residual_out, T_valid)
+                      residual_out, T_valid,
+                      host=bool(options is not None and options.host_buffers),
+                      addend=getattr(options, "_addend_ref", None),
+                      scale_layout=options.scale_layout if options is not None else 0)
     st = load_library().sp_fused_reduce_norm_ex(
         ctypes.byref(options) if options is not None else None, *args, _stream_handle(stream))
     if st != 0:
@@ -226,7 +296,7 @@ def sp_fused_reduce_norm_host(partials, weight, out, residual_out, *, residual=N
     one element, or None. Asynchronous on ``stream`` (default: torch's current CUDA stream);
     synchronise before reading the outputs."""
     args = _main_args(partials, residual, weight, bias, eps, quant_mode, scale, out, out_scales,
-                      residual_out, T_valid)
+                      residual_out, T_valid, host=True)
     st = load_library().sp_fused_reduce_norm_host(*args, _stream_handle(stream))
     if st != 0:
         raise SpError(st, "sp_fused_reduce_norm_host")
@@ -290,7 +360,13 @@ def sp_out_scales_bytes_ex(T_pad: int, H: int, quant_mode, scale_layout: int) ->
 def sp_fc2_reorganize(x, otp_size: int, y, stream=None) -> None:
     """FlashComm2 token reorganisation of x [G, N, H/G] into y [G, N/D, H/P] (CUDA tensors of
     the same dtype; D = G / otp_size)."""
+    import torch
+    if not isinstance(x, torch.Tensor) or x.dim() != 3:
+        raise ValueError("x: expected a tensor [G, N, H/G]")
     G, N, F = x.shape
+    dev = _current_device()
+    _check_tensor("x", x, (x.dtype,), 0, dev, False)
+    _check_tensor("y", y, (x.dtype,), x.numel() * x.element_size(), dev, False)
     st = load_library().sp_fc2_reorganize(x.data_ptr(), G, otp_size, N, F * G, x.element_size(),
                                           y.data_ptr(), _stream_handle(stream))
     if st != 0:
