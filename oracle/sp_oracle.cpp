@@ -181,9 +181,10 @@ int64_t out_bytes(const Args& a) {
 // scaling factors" layout): the [rows][cols] scale matrix is padded to multiples of 128 rows and
 // 4 columns; tile (i, j) = rows 128i.., columns 4j.. is a 512-byte block at (i * tiles_per_row + j)
 // * 512; inside it, row r and column c sit at (r % 32) * 16 + (r / 32) * 4 + c.
-// On the CPU this map is pinned only by the permutation property (every row-major scale once,
-// padding zero); a GPU test pins the placement itself by feeding the library's output, whose
-// parity with this function is tested, to cuBLASLt's block-scaled NVFP4 GEMM.
+// Pinned on the CPU by PyTorch's own construction of this layout (a reshape/permute of the
+// row-major scale matrix) and by the permutation property (every row-major scale once, padding
+// zero); on the GPU cuBLASLt's block-scaled NVFP4 GEMM reads the library's output, whose parity
+// with this function is tested.
 int64_t swizzled_rows(int64_t T_pad) { return (T_pad + 127) / 128 * 128; }
 int64_t swizzled_cols(int64_t H) { return (H / 16 + 3) / 4 * 4; }
 int64_t swizzled_offset(int64_t row, int64_t col, int64_t H) {

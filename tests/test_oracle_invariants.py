@@ -486,3 +486,44 @@ def test_swizzled_scales_hold_exactly_the_row_major_scales(T, H):
     want = np.bincount(flat["out_scales"].ravel(), minlength=256)
     want[0] += rows * cols - T_pad * (H // 16)
     assert np.array_equal(np.bincount(swz["out_scales"], minlength=256), want)
+
+
+def _torch_to_blocked():
+    """PyTorch's own helper that rearranges a block-scale matrix into the 128x4-tile layout
+    block-scaled GEMMs read (torch/testing/_internal/common_quantized.py, ``to_blocked``, written
+    after the cuBLAS "1D block scaling factors layout" description). Its module imports test-only
+    packages, so the two functions are taken from PyTorch's source file and run as they stand."""
+    import ast
+    path = os.path.join(os.path.dirname(torch.__file__), "testing", "_internal",
+                        "common_quantized.py")
+    if not os.path.exists(path):
+        pytest.skip("this PyTorch has no common_quantized.py")
+    with open(path) as f:
+        tree = ast.parse(f.read())
+    fns = [n for n in tree.body
+           if isinstance(n, ast.FunctionDef) and n.name in ("ceil_div", "to_blocked")]
+    if len(fns) != 2:
+        pytest.skip("this PyTorch has no to_blocked helper")
+    ns = {"torch": torch}
+    exec(compile(ast.Module(body=fns, type_ignores=[]), path, "exec"), ns)
+    return ns["to_blocked"]
+
+
+@pytest.mark.parametrize("T,H", [(8, 64), (130, 80), (256, 1024), (3, 16), (300, 2000)])
+def test_swizzled_scales_match_torch_blocked_layout(T, H):
+    """The placement itself, pinned without a GPU: the oracle's swizzled scale buffer equals
+    PyTorch's independent reshape/permute construction of the same layout applied to the oracle's
+    row-major scales (padding bytes zero in both)."""
+    to_blocked = _torch_to_blocked()
+    g = torch.Generator().manual_seed(7 * T + H)
+    tp = 2
+    T_pad = tp * -(-T // tp)
+    partials = rand_bf16(g, (tp, T_pad, H), 0.7)
+    residual = rand_bf16(g, (T_pad, H))
+    w, b = rand_bf16(g, (H,), 0.1) + 1, rand_bf16(g, (H,), 0.01)
+    args = (bits(partials), bits(residual), bits(w), bits(b), 1e-6, "nvfp4", 60.0, T)
+    flat = oracle.fused_reduce_norm(*args)
+    swz = oracle.fused_reduce_norm(*args, scale_layout=1)
+    assert flat["status"] == 0 and swz["status"] == 0
+    want = to_blocked(torch.from_numpy(flat["out_scales"].reshape(T_pad, H // 16).copy()))
+    assert np.array_equal(swz["out_scales"], want.numpy())

@@ -44,6 +44,7 @@ MUTANTS = {
     "bf16_saturates": ("std::ldexp(255.0, 120), false}", "std::ldexp(255.0, 120), true}"),
     "fc2_contiguous_batch_ids": ("ids[j * P + k] = j + k * D;", "ids[j * P + k] = j * P + k;"),
     "fc2_member_order": ("out + i * row_out + m * row_in", "out + i * row_out + (D - 1 - m) * row_in"),
+    "swizzle_row_terms_swapped": ("(r % 32) * 16 + (r / 32) * 4 + c", "(r / 32) * 16 + (r % 32) * 4 + c"),
     "residual_out_unrounded_sum": ("a.residual_out[t * H + j] = bf16_code(h[j]);",
                                    "a.residual_out[t * H + j] = bf16_code(h[j] - bf16_value(a.weight[j]) + 1.0);"),
 }
