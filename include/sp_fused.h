@@ -83,6 +83,14 @@ typedef enum sp_quant_mode {
  * Rows t >= T_valid are padding: none of their inputs is read and every byte of their out,
  * out_scales and residual_out rows is written as zero.
  *
+ * Restates: the sum over partials is the ReduceScatter's element-wise sum split along tokens
+ * (LongCat-Flash A3 page, o_proj TP paragraph; vllm-ascend SP/FlashComm notes §2.1-§2.2); bias,
+ * residual, new residual and RMSNorm with weight follow the add-RMSNorm-bias replacement
+ * (vllm-ascend SP/FlashComm notes §2.3); the quantisers are the local quant after the norm and
+ * their shard-local scales (vLLM SP/AsyncTP/quant notes §四); T_pad is the token count padded to
+ * a multiple of tp (vllm-ascend SP/FlashComm notes §2.4) and padding rows are zeroed after the
+ * reduction (PR #18671 notes §5.2-§5.3).
+ *
  * Arguments:
  *   partials     bf16 [tp][T_pad][H]: partial r holds rank r's un-reduced output for every token.
  *   tp           number of partials, >= 1.
@@ -119,7 +127,9 @@ sp_status sp_fused_reduce_norm(const void* partials, int tp, int64_t T_pad, int6
 /*
  * sp_check_args — the argument checks of sp_fused_reduce_norm alone, in the same order and with
  * the same statuses. Pointers are only compared, never dereferenced; touches no GPU and needs
- * no CUDA device.
+ * no CUDA device. The shape rules are the single-GPU form of the shard checks that raise on a
+ * layout mismatch (PR #18671 notes §5.2); the refusal of dynamic per-tensor FP8 is the
+ * per-tensor correctness table (vLLM SP/AsyncTP/quant notes §四).
  */
 sp_status sp_check_args(const void* partials, int tp, int64_t T_pad, int64_t T_valid, int64_t H,
                         const void* residual, const void* weight, const void* bias, float eps,
@@ -178,12 +188,16 @@ typedef struct sp_fused_options {
   const struct sp_launch_config* launch;
 } sp_fused_options;
 
+/* sp_options_init — the defaults (exactly sp_fused_reduce_norm). The options restate PR #18671
+ * notes §5.3 (partial_scale) and vllm-ascend SP/FlashComm notes §2.3 (addend). */
 void sp_options_init(sp_fused_options* options /* host, out */);
 
 /*
  * sp_fused_reduce_norm_ex — sp_fused_reduce_norm with options (NULL options = defaults). The
  * addend follows the same rules as the residual (16-byte aligned, may not overlap an output).
- * A non-finite partial_scale is SP_ERR_INVALID_ARG.
+ * A non-finite partial_scale is SP_ERR_INVALID_ARG. Restates, beyond sp_fused_reduce_norm: the
+ * output scale applied to each rank's partial before the ReduceScatter (PR #18671 notes §5.3) and
+ * the per-shard addend added after it (vllm-ascend SP/FlashComm notes §2.3, deepstack rewrite).
  */
 sp_status sp_fused_reduce_norm_ex(const sp_fused_options* options /* host */,
                                   const void* partials, int tp, int64_t T_pad, int64_t T_valid,
@@ -192,7 +206,8 @@ sp_status sp_fused_reduce_norm_ex(const sp_fused_options* options /* host */,
                                   void* out, void* out_scales, void* residual_out,
                                   sp_stream_t stream);
 
-/* sp_check_args_ex — the checks of sp_fused_reduce_norm_ex alone (no GPU needed). */
+/* sp_check_args_ex — the checks of sp_fused_reduce_norm_ex alone (no GPU needed); the same
+ * passages as sp_check_args (PR #18671 notes §5.2) plus the option rules above. */
 sp_status sp_check_args_ex(const sp_fused_options* options /* host */, const void* partials,
                            int tp, int64_t T_pad, int64_t T_valid, int64_t H, const void* residual,
                            const void* weight, const void* bias, float eps, int quant_mode,
@@ -207,7 +222,9 @@ sp_status sp_check_args_ex(const sp_fused_options* options /* host */, const voi
  * and device->host traffic of a call overlap each other and the computation, with no device
  * staging buffers. Same arguments, checks, statuses and results as sp_fused_reduce_norm, plus
  * SP_ERR_INVALID_ARG for a pointer the device cannot reach (pageable memory). Asynchronous on
- * `stream`: synchronise the stream before reading the outputs on the host.
+ * `stream`: synchronise the stream before reading the outputs on the host. The stage is the one
+ * sp_fused_reduce_norm restates (vllm-ascend SP/FlashComm notes §2.3; vLLM SP/AsyncTP/quant
+ * notes §四); host-resident buffers have no counterpart on the pages.
  */
 sp_status sp_fused_reduce_norm_host(const void* partials, int tp, int64_t T_pad, int64_t T_valid,
                                     int64_t H, const void* residual, const void* weight,
@@ -236,6 +253,8 @@ sp_status sp_fused_reduce_norm_host(const void* partials, int tp, int64_t T_pad,
  *                   `split` times as many SMs. Grid = split x min(T rows, SMs x ctas_per_sm /
  *                   split) CTAs. Another value is SP_ERR_INVALID_ARG; split > 1 with the STAGED
  *                   kernel or vec_per_thread 4 is SP_ERR_UNSUPPORTED.
+ * Launch shapes are this library's choice for GB300 and have no counterpart on the pages (their
+ * fused operators are Ascend kernels); the function computed is sp_fused_reduce_norm's.
  */
 enum { SP_KERNEL_STAGED = 0, SP_KERNEL_DIRECT = 1 };
 
@@ -268,6 +287,8 @@ sp_status sp_fused_reduce_norm_with_config(const sp_launch_config* config /* hos
  *   sp_out_bytes / sp_out_scales_bytes(_ex): sizes of `out` and `out_scales` for a mode (and a
  *       scale layout; 0 for no buffer), or -1 for an invalid mode or layout.
  *   sp_max_hidden: the largest H the kernels take.
+ * Buffer sizes follow the layouts of sp_fused_reduce_norm (vLLM SP/AsyncTP/quant notes §四 for
+ * the per-token and per-block scales).
  */
 int64_t sp_pad_tokens(int64_t T, int tp);
 sp_status sp_shard_rows(int64_t T_pad, int tp, int rank, int64_t* start /* host */,
@@ -297,10 +318,12 @@ sp_status sp_fc2_reorganize(const void* x, int global_tp, int otp_size, int64_t 
                             int elem_bytes, void* y, sp_stream_t stream);
 sp_status sp_fc2_check_args(const void* x, int global_tp, int otp_size, int64_t N, int64_t H,
                             int elem_bytes, const void* y);
-/* The reorganised batch ids: ids[j*P + k] = j + k*D (D lists of P segments; host array). */
+/* The reorganised batch ids: ids[j*P + k] = j + k*D (D lists of P segments; host array), the
+ * reorgnized_batch_ids of vllm-ascend SP/FlashComm notes §4.4. */
 sp_status sp_fc2_batch_ids(int global_tp, int otp_size, int* ids /* host, [D*P] */);
 
-/* Name of a status code, e.g. "SP_ERR_ALIGNMENT"; "SP_UNKNOWN_STATUS" for other values. */
+/* Name of a status code, e.g. "SP_ERR_ALIGNMENT"; "SP_UNKNOWN_STATUS" for other values. A
+ * utility with no counterpart on the pages. */
 const char* sp_status_string(int status);
 
 /*
@@ -308,9 +331,9 @@ const char* sp_status_string(int status);
  * their shared-memory rings are bounded in time; a wait that runs out (which only a hardware or
  * runtime fault could cause) sets SP_DEVICE_ERR_WAIT_TIMEOUT here, abandons the launch after
  * letting its copies in flight land, and the rows (or output tiles) it had not finished hold
- * undefined values. sp_device_error reads (and, when
- * `clear` is non-zero, resets) the word of the current device; it synchronises with the
- * device. SP_ERR_CUDA if the runtime call fails.
+ * undefined values. sp_device_error reads (and, when `clear` is non-zero, resets) the word of
+ * the current device; it synchronises with the device. SP_ERR_CUDA if the runtime call fails.
+ * Failure reporting of this library, with no counterpart on the pages.
  */
 enum { SP_DEVICE_ERR_WAIT_TIMEOUT = 1 };
 sp_status sp_device_error(uint32_t* flags /* host, out */, int clear);
@@ -320,7 +343,7 @@ sp_status sp_device_error(uint32_t* flags /* host, out */, int clear);
  * with a limit of `limit_ns` (1 ns .. 2 s), on a shared-memory barrier that nothing completes;
  * the wait gives up, sets SP_DEVICE_ERR_WAIT_TIMEOUT in the device error word and the kernel
  * ends normally (the context stays usable). Asynchronous on `stream`; SP_ERR_INVALID_ARG for a
- * limit out of range.
+ * limit out of range. A test hook with no counterpart on the pages.
  */
 sp_status sp_selftest_wait_timeout(uint64_t limit_ns, sp_stream_t stream);
 

@@ -379,3 +379,20 @@ def test_every_selected_launch_passes_the_launch_checks(lib):
                     assert sp.sp_status_string(st) == "SP_OK", (mode, tp, H, T, cfg.as_dict())
                     checked += 1
     assert checked > 9000
+
+
+def test_each_declared_call_cites_its_passage():
+    """Every exported call's comment (the comment block nearest before its declaration) names
+    the passage of the pages it restates (a section mark), or says it has no counterpart there."""
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        src = open(h).read()
+        # comment blocks that open a line (argument notes inside a declaration are not blocks)
+        pieces = re.split(r"(^[ \t]*/\*.*?\*/)", src, flags=re.S | re.M)
+        last_comment = ""
+        for piece in pieces:
+            if piece.lstrip().startswith("/*"):
+                last_comment = piece
+                continue
+            for name in re.findall(r"^\s*(?:const\s+)?[A-Za-z_][\w\s\*]*?\b(sp_\w+)\s*\(", piece,
+                                   flags=re.M):
+                assert "§" in last_comment or "no counterpart on the pages" in last_comment, name
