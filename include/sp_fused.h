@@ -162,17 +162,35 @@ sp_status sp_check_args(const void* partials, int tp, int64_t T_pad, int64_t T_v
  *                  rows (applies to the staged kernel, the one device-buffer calls use).
  *                  SP_SCHEDULE_AUTO (the default): dynamic when the staged kernel gives every CTA
  *                  at least 10 rows, H >= 2048 and (tp + 3) * 2H >= 24 KB, static otherwise.
- *                  The counters are a fixed table in the library's device memory (no allocation):
- *                  one slot per stream (told apart by cudaStreamGetId), reset by each call's last
- *                  CTA, so calls on one stream reuse it in stream order and calls on different
- *                  streams never share one. A call falls back to the static schedule while its
- *                  stream is being captured into a CUDA graph (a replay may run beside calls on
- *                  the capturing stream) and when all slots are taken. Any other value is
- *                  SP_ERR_UNSUPPORTED.
+ *                  Without row_counter (below) the counters are a fixed table of 256 slots in
+ *                  the library's device memory (no allocation): one slot per stream (told apart
+ *                  by cudaStreamGetId), reset by each call's last CTA, so calls on one stream
+ *                  reuse it in stream order and calls on different streams never share one.
+ *                  Slots are held for the life of the process: a process that has used 256
+ *                  streams on a device runs the static schedule on every later stream (same
+ *                  results, up to ~13 % slower on large calls) unless it passes row_counter. A
+ *                  call also falls back to the static schedule while its stream is being
+ *                  captured into a CUDA graph (a replay may run beside calls on the capturing
+ *                  stream), again unless it passes row_counter. sp_last_launch tells which
+ *                  schedule a call ran. Any other value is SP_ERR_UNSUPPORTED.
  *   launch         a launch configuration (below) to run instead of the one sp_select_launch
  *                  picks, for tests and tuning; NULL (the default) = the library's choice. The
  *                  checks of sp_fused_reduce_norm_with_config apply. With host_buffers = 1 it
  *                  must name the DIRECT kernel (else SP_ERR_UNSUPPORTED).
+ *   row_counter    NULL (the default), or the caller's own device buffer of two uint32 (8 bytes,
+ *                  16-byte aligned, zero before its first use) that the dynamic schedule claims
+ *                  rows from instead of the library's per-stream table. Each call leaves it zero
+ *                  when it completes, so it can be reused by calls that are ordered one after the
+ *                  other (one stream, or graph replays that do not overlap); calls that overlap
+ *                  on the GPU must not share one. Used also while the stream is being captured.
+ *                  After a call whose status reports a timeout, zero it again before reuse.
+ *   status         NULL (the default), or a device uint32 (16-byte aligned) that the call ORs
+ *                  its device-side error bits into (SP_DEVICE_ERR_WAIT_TIMEOUT) in place of the
+ *                  device error word of sp_device_error, in stream order: read it once the
+ *                  call's work on the stream has completed (a copy on the same stream, or after
+ *                  a synchronisation). The library never clears it. When a bit is set, that
+ *                  call's outputs are undefined.
+ *                  row_counter and status may not overlap any input or output of the call.
  */
 enum { SP_SCALES_ROW_MAJOR = 0, SP_SCALES_SWIZZLED_128X4 = 1 };
 enum { SP_SCHEDULE_AUTO = 0, SP_SCHEDULE_STATIC = 1, SP_SCHEDULE_DYNAMIC = 2 };
@@ -186,6 +204,8 @@ typedef struct sp_fused_options {
   int host_buffers;
   int schedule;
   const struct sp_launch_config* launch;
+  void* row_counter;
+  uint32_t* status;
 } sp_fused_options;
 
 /* sp_options_init — the defaults (exactly sp_fused_reduce_norm). The options restate PR #18671
@@ -278,6 +298,22 @@ sp_status sp_fused_reduce_norm_with_config(const sp_launch_config* config /* hos
                                            sp_stream_t stream);
 
 /*
+ * sp_last_launch — what the calling thread's last successful fused-stage call launched: the
+ * configuration (stages resolved), the CTAs launched and the row schedule it ran
+ * (SP_SCHEDULE_STATIC or SP_SCHEDULE_DYNAMIC; the direct kernel is always static). All zero
+ * before the first such call on this thread. Host only; SP_ERR_INVALID_ARG for a NULL pointer.
+ * Lets a caller see, for instance, that a call fell back to the static schedule. A utility with
+ * no counterpart on the pages.
+ */
+typedef struct sp_launch_info {
+  sp_launch_config config;
+  int grid;
+  int schedule;
+} sp_launch_info;
+
+sp_status sp_last_launch(sp_launch_info* info /* host, out */);
+
+/*
  * Layout helpers (host only, no device use).
  *   sp_pad_tokens: the smallest multiple of tp that is >= T (token padding before the
  *       ReduceScatter; vllm-ascend SP notes §2.4, §3.3), or -1 if T < 0 or tp < 1.
@@ -329,9 +365,10 @@ const char* sp_status_string(int status);
 /*
  * Device-side error word. The waits of the staged kernel and of the reorganisation kernel on
  * their shared-memory rings are bounded in time; a wait that runs out (which only a hardware or
- * runtime fault could cause) sets SP_DEVICE_ERR_WAIT_TIMEOUT here, abandons the launch after
- * letting its copies in flight land, and the rows (or output tiles) it had not finished hold
- * undefined values. sp_device_error reads (and, when `clear` is non-zero, resets) the word of
+ * runtime fault could cause) sets SP_DEVICE_ERR_WAIT_TIMEOUT here (or, for a call that passed a
+ * status word in its options, in that word instead), abandons the launch after letting its
+ * copies in flight land, and the rows (or output tiles) it had not finished hold undefined
+ * values. sp_device_error reads (and, when `clear` is non-zero, resets) the word of
  * the current device; it synchronises with the device. SP_ERR_CUDA if the runtime call fails.
  * Failure reporting of this library, with no counterpart on the pages.
  */
@@ -346,6 +383,29 @@ sp_status sp_device_error(uint32_t* flags /* host, out */, int clear);
  * limit out of range. A test hook with no counterpart on the pages.
  */
 sp_status sp_selftest_wait_timeout(uint64_t limit_ns, sp_stream_t stream);
+
+/*
+ * sp_selftest_fused_timeout — the fused stage's own abort path on the GPU, without a fault. The
+ * call runs like sp_fused_reduce_norm_ex with `options` on the staged kernel with two vectors
+ * per consumer thread (so H <= 8192; options->launch, if given, must name that kernel and
+ * vec_per_thread 2; host_buffers must be 0; else SP_ERR_UNSUPPORTED), except that every bounded
+ * wait of the launch
+ * gives up after `limit_ns` (1 ns .. 2 s) and the producer of CTA 0 never fills ring stage number
+ * `withhold` (counted from 0 in the order it fills stages: with the dynamic schedule each row's
+ * first stage also carries its index) and issues nothing after it. The consumer warps' waits on
+ * that stage run out, all of them leave together, the producer's drain of it runs out too, and
+ * the launch ends with SP_DEVICE_ERR_WAIT_TIMEOUT in the options' status word (or, without one,
+ * in the device error word); the context stays usable and the outputs are undefined. If CTA 0 fills fewer
+ * stages than `withhold`, nothing runs out. Asynchronous on `stream`; SP_ERR_INVALID_ARG for a
+ * limit out of range or a negative `withhold`. A test hook with no counterpart on the pages.
+ */
+sp_status sp_selftest_fused_timeout(uint64_t limit_ns, int64_t withhold,
+                                    const sp_fused_options* options /* host */,
+                                    const void* partials, int tp, int64_t T_pad, int64_t T_valid,
+                                    int64_t H, const void* residual, const void* weight,
+                                    const void* bias, float eps, int quant_mode,
+                                    const float* scale, void* out, void* out_scales,
+                                    void* residual_out, sp_stream_t stream);
 
 #ifdef __cplusplus
 }

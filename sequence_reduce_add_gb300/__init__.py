@@ -25,6 +25,7 @@ __all__ = [
     "sp_device_error", "allocate_outputs", "LaunchConfig", "Options", "sp_options_init",
     "sp_fused_reduce_norm_ex", "sp_check_args_ex", "sp_out_scales_bytes_ex", "sp_fc2_reorganize",
     "sp_fc2_check_args", "sp_fc2_batch_ids", "sp_selftest_wait_timeout",
+    "sp_selftest_fused_timeout", "sp_last_launch", "LaunchInfo",
 ]
 
 QUANT_MODES = {"none": 0, "fp8_static": 1, "fp8_per_token": 2, "nvfp4": 3,
@@ -57,10 +58,17 @@ class LaunchConfig(ctypes.Structure):
 
 class Options(ctypes.Structure):
     """sp_fused_options: partial_scale, addend (device address or None), scale_layout,
-    host_buffers, schedule, launch (a LaunchConfig or None)."""
+    host_buffers, schedule, launch (a LaunchConfig or None), row_counter (the caller's own
+    dynamic-schedule counter, 8 bytes, or None), status (a per-call error word or None)."""
     _fields_ = [("partial_scale", ctypes.c_float), ("addend", ctypes.c_void_p),
                 ("scale_layout", ctypes.c_int), ("host_buffers", ctypes.c_int),
-                ("schedule", ctypes.c_int), ("launch", ctypes.POINTER(LaunchConfig))]
+                ("schedule", ctypes.c_int), ("launch", ctypes.POINTER(LaunchConfig)),
+                ("row_counter", ctypes.c_void_p), ("status", ctypes.c_void_p)]
+
+
+class LaunchInfo(ctypes.Structure):
+    """sp_launch_info: the configuration a call launched, its grid and its row schedule."""
+    _fields_ = [("config", LaunchConfig), ("grid", ctypes.c_int), ("schedule", ctypes.c_int)]
 
 
 SCHEDULES = {"auto": 0, "static": 1, "dynamic": 2}
@@ -130,6 +138,11 @@ def load_library() -> ctypes.CDLL:
     lib.sp_device_error.restype = ctypes.c_int
     lib.sp_selftest_wait_timeout.argtypes = [ctypes.c_uint64, _vp]
     lib.sp_selftest_wait_timeout.restype = ctypes.c_int
+    lib.sp_selftest_fused_timeout.argtypes = ([ctypes.c_uint64, _i64, ctypes.POINTER(Options)]
+                                              + _MAIN_ARGS + [_vp])
+    lib.sp_selftest_fused_timeout.restype = ctypes.c_int
+    lib.sp_last_launch.argtypes = [ctypes.POINTER(LaunchInfo)]
+    lib.sp_last_launch.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -243,15 +256,22 @@ def sp_fused_reduce_norm(partials, weight, out, residual_out, *, residual=None, 
 
 
 def sp_options_init(*, partial_scale: float = 1.0, addend=None, scale_layout: int = 0,
-                    host_buffers: bool = False, schedule="auto", launch=None) -> Options:
+                    host_buffers: bool = False, schedule="auto", launch=None, row_counter=None,
+                    status=None) -> Options:
     """An sp_fused_options initialised by the library, then set from the keywords (``addend`` is a
     tensor or None; ``schedule`` is "auto", "static", "dynamic" or the enum value; ``launch`` a
-    LaunchConfig, a dict of its fields, or None for the library's choice)."""
+    LaunchConfig, a dict of its fields, or None for the library's choice; ``row_counter`` an
+    int32/uint32 tensor of two zeroed elements or None; ``status`` an int32/uint32 tensor of one
+    element or None)."""
     o = Options()
     load_library().sp_options_init(ctypes.byref(o))
     o.partial_scale = partial_scale
     o.addend = _ptr(addend)
     o._addend_ref = addend  # checked (and kept alive) by the call that uses these options
+    o.row_counter = _ptr(row_counter)
+    o._row_counter_ref = row_counter
+    o.status = _ptr(status)
+    o._status_ref = status
     o.scale_layout = scale_layout
     o.host_buffers = 1 if host_buffers else 0
     o.schedule = SCHEDULES[schedule] if isinstance(schedule, str) else int(schedule)
@@ -268,15 +288,56 @@ def sp_fused_reduce_norm_ex(options: Options | None, partials, weight, out, resi
                             stream=None) -> None:
     """``sp_fused_reduce_norm`` with options (``sp_options_init``): a scale applied to every
     partial before the reduction, an addend after it, host buffers."""
-    args = _main_args(partials, residual, weight, bias, eps, quant_mode, scale, out, out_scales,
-                      residual_out, T_valid,
-                      host=bool(options is not None and options.host_buffers),
-                      addend=getattr(options, "_addend_ref", None),
-                      scale_layout=options.scale_layout if options is not None else 0)
+    args = _options_args(options, partials, residual, weight, bias, eps, quant_mode, scale, out,
+                         out_scales, residual_out, T_valid)
     st = load_library().sp_fused_reduce_norm_ex(
         ctypes.byref(options) if options is not None else None, *args, _stream_handle(stream))
     if st != 0:
         raise SpError(st, "sp_fused_reduce_norm_ex")
+
+
+def _options_args(options, partials, residual, weight, bias, eps, quant_mode, scale, out,
+                  out_scales, residual_out, T_valid):
+    """_main_args for the options-taking calls: the options' tensors are checked too."""
+    host = bool(options is not None and options.host_buffers)
+    args = _main_args(partials, residual, weight, bias, eps, quant_mode, scale, out, out_scales,
+                      residual_out, T_valid, host=host,
+                      addend=getattr(options, "_addend_ref", None),
+                      scale_layout=options.scale_layout if options is not None else 0)
+    import torch
+    words = (torch.int32, torch.uint32) if hasattr(torch, "uint32") else (torch.int32,)
+    for name, need in (("row_counter", 8), ("status", 4)):
+        t = getattr(options, f"_{name}_ref", None)
+        if t is not None:
+            _check_tensor(name, t, words, need, _current_device(), host)
+    return args
+
+
+def sp_selftest_fused_timeout(limit_ns: int, withhold: int, options: Options | None, partials,
+                              weight, out, residual_out, *, residual=None, bias=None,
+                              eps: float = 1e-6, quant_mode="none", scale=None, out_scales=None,
+                              T_valid: int | None = None, stream=None) -> None:
+    """The staged kernel's abort path, forced without a fault (see include/sp_fused.h): waits
+    give up after ``limit_ns`` and CTA 0 never fills ring stage ``withhold``."""
+    args = _options_args(options, partials, residual, weight, bias, eps, quant_mode, scale, out,
+                         out_scales, residual_out, T_valid)
+    st = load_library().sp_selftest_fused_timeout(
+        limit_ns, withhold, ctypes.byref(options) if options is not None else None, *args,
+        _stream_handle(stream))
+    if st != 0:
+        raise SpError(st, "sp_selftest_fused_timeout")
+
+
+def sp_last_launch() -> dict:
+    """The calling thread's last fused-stage launch: {"config": {...}, "grid", "schedule"}
+    (schedule "static" or "dynamic"; None before the first call)."""
+    info = LaunchInfo()
+    st = load_library().sp_last_launch(ctypes.byref(info))
+    if st != 0:
+        raise SpError(st, "sp_last_launch")
+    names = {1: "static", 2: "dynamic"}
+    return {"config": info.config.as_dict(), "grid": info.grid,
+            "schedule": names.get(info.schedule)}
 
 
 def sp_check_args_ex(options: Options | None, partials, tp, T_pad, T_valid, H, residual, weight,

@@ -46,9 +46,14 @@ struct Params {
   int seg_stride;             // staged kernel: bytes between ring stages (2H rounded up to 128)
   int wb_offset;              // staged kernel: byte offset of the weight/bias copy [2][H] bf16
   int ring_offset;            // staged kernel: byte offset of the ring in dynamic shared memory
-  int counter_slot;           // dynamic schedule: row counter slot of the launch's stream
+  unsigned int* row_counter;  // dynamic schedule: [next claim, CTAs done], zero between calls
+  unsigned int* error_word;   // where a timed-out wait is reported: the call's status word, or
+                              // else g_error_flags (the device error word)
+  uint64_t wait_limit_ns;     // every bounded wait gives up after this long
+  int64_t withhold;           // self-test only: CTA 0 skips its ring fill of this issue number
   int split_chunk;            // split rows: 16-byte vectors of a row per CTA of the cluster
 };
+
 
 // Per-warp slot of the row reduction: sum of squares, max |h*w| and an abort vote.
 struct __align__(16) RedSlot {

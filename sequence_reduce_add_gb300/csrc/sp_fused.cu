@@ -63,6 +63,10 @@ struct Extras {
   const void* addend = nullptr;
   int scale_layout = SP_SCALES_ROW_MAJOR;
   int schedule = SP_SCHEDULE_AUTO;
+  void* row_counter = nullptr;      // the caller's own [next claim, CTAs done] pair, or null
+  uint32_t* status = nullptr;       // the caller's per-call error word, or null
+  uint64_t wait_limit_ns = spk::kWaitLimitNs;
+  int64_t withhold = -1;            // self-test: CTA 0 withholds this ring fill (else -1)
 };
 
 sp_status check(const void* partials, int tp, int64_t T_pad, int64_t T_valid, int64_t H,
@@ -90,19 +94,20 @@ sp_status check(const void* partials, int tp, int64_t T_pad, int64_t T_valid, in
   const int64_t rows = T_pad * H * 2;
   const void* inputs[] = {partials, residual, weight, bias, scale, x.addend};
   const int64_t in_n[] = {rows * tp, rows, H * 2, H * 2, 4, rows};
-  const void* outputs[] = {out, out_scales, residual_out};
+  // everything the kernel writes: the outputs, the caller's row counter and status word
+  const void* outputs[] = {out, out_scales, residual_out, x.row_counter, x.status};
   const int64_t out_n[] = {out_bytes_of(T_pad, H, mode),
-                           scale_bytes_of(T_pad, H, mode, x.scale_layout), rows};
-  for (int o = 0; o < 3; ++o) {
+                           scale_bytes_of(T_pad, H, mode, x.scale_layout), rows, 8, 4};
+  for (int o = 0; o < 5; ++o) {
     for (int i = 0; i < 6; ++i) {
       if (o == 2 && i == 1 && residual_out == residual) continue;  // in-place residual update
       if (overlaps(outputs[o], out_n[o], inputs[i], in_n[i])) return SP_ERR_INVALID_ARG;
     }
-    for (int q = o + 1; q < 3; ++q)
+    for (int q = o + 1; q < 5; ++q)
       if (overlaps(outputs[o], out_n[o], outputs[q], out_n[q])) return SP_ERR_INVALID_ARG;
   }
-  const void* all[] = {partials, residual, weight, bias,         scale,
-                       out,      out_scales, residual_out, x.addend};
+  const void* all[] = {partials, residual,     weight,   bias,          scale,   out,
+                       out_scales, residual_out, x.addend, x.row_counter, x.status};
   for (const void* ptr : all)
     if (ptr && !aligned16(ptr)) return SP_ERR_ALIGNMENT;
   if (H > kMaxHidden) return SP_ERR_UNSUPPORTED;
@@ -127,7 +132,10 @@ struct DeviceInfo {
   std::atomic<int> sms{0};
   std::atomic<bool> staged_attr_set[3][4][2] = {};
   std::atomic<bool> fc2_attr_set{false};
-  // Row counter slots of the dynamic schedule: slot i belongs to the stream with id slot_stream[i].
+  // Row counter slots of the dynamic schedule: slot i belongs to the stream with id slot_stream[i];
+  // `counters` is the device address of the table (spk::g_row_counters) in this device's context.
+  unsigned int* counters = nullptr;
+  unsigned int* error_word = nullptr;  // device address of spk::g_error_flags
   std::mutex slot_mutex;
   unsigned long long slot_stream[spk::kRowCounterSlots] = {};
   int slots_used = 0;
@@ -145,6 +153,12 @@ sp_status device_info(DeviceInfo** info) {
       int sms = 0;
       if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
         return SP_ERR_CUDA;
+      void* counters = nullptr;
+      if (cudaGetSymbolAddress(&counters, spk::g_row_counters) != cudaSuccess) return SP_ERR_CUDA;
+      d.counters = static_cast<unsigned int*>(counters);
+      void* error_word = nullptr;
+      if (cudaGetSymbolAddress(&error_word, spk::g_error_flags) != cudaSuccess) return SP_ERR_CUDA;
+      d.error_word = static_cast<unsigned int*>(error_word);
       d.id = dev;
       d.sms.store(sms, std::memory_order_release);
     }
@@ -327,6 +341,9 @@ cudaError_t set_staged_smem_limit(DeviceInfo* dev) {
   return e;
 }
 
+// What the calling thread's last successful launch was (sp_last_launch).
+thread_local sp_launch_info t_last_launch{};
+
 // Split rows: clusters of `split` CTAs (one row each at a time), as many as the SMs hold at the
 // requested CTAs per SM, and never more than rows; launched with PDL like the rest.
 template <int kVec, int kMode, int kSplit, int kBatch>
@@ -355,6 +372,7 @@ cudaError_t launch_split(const sp_launch_config& cfg, const spk::Params& p, cuda
   attr[1].val.clusterDim.z = 1;
   lc.attrs = attr;
   lc.numAttrs = 2;
+  t_last_launch.grid = static_cast<int>(clusters * kSplit);
   e = cudaLaunchKernelEx(&lc, kernel, p);
   return e != cudaSuccess ? e : cudaGetLastError();
 }
@@ -369,6 +387,7 @@ cudaError_t launch_direct(const sp_launch_config& cfg, spk::Params& p, cudaStrea
     int grid = 0;
     cudaError_t e = persistent_grid(kernel, p.nthreads, 0, cfg.ctas_per_sm, p.T_pad, dev, &grid);
     if (e != cudaSuccess) return e;
+    t_last_launch.grid = grid;
     e = launch_pdl(kernel, grid, p.nthreads, 0, stream, p);
     return e != cudaSuccess ? e : cudaGetLastError();
   }
@@ -396,9 +415,10 @@ cudaError_t launch_direct_batched(const sp_launch_config& cfg, spk::Params& p,
 }
 
 template <int kVec, int kMode>
-cudaError_t launch_one(const sp_launch_config& cfg, spk::Params& p, int smem, int schedule,
+cudaError_t launch_one(const sp_launch_config& cfg, spk::Params& p, int smem, const Extras& x,
                        cudaStream_t stream, DeviceInfo* dev) {
   int grid = 0;
+  const int schedule = x.schedule;
   if (cfg.kernel == SP_KERNEL_DIRECT) {
     if constexpr (kVec <= 2) {
       switch (split_of(cfg)) {
@@ -416,14 +436,23 @@ cudaError_t launch_one(const sp_launch_config& cfg, spk::Params& p, int smem, in
   e = persistent_grid(spk::k_staged<kVec, kMode, false>, threads, smem, cfg.ctas_per_sm, p.T_pad,
                       dev, &grid);
   if (e != cudaSuccess) return e;
-  int slot = -1;
+  unsigned int* counter = nullptr;
   const bool want_dynamic =
       schedule == SP_SCHEDULE_DYNAMIC ||
       (schedule == SP_SCHEDULE_AUTO && p.rows_total >= kDynamicMinRowsPerCta * grid &&
        p.H >= kDynamicMinHidden &&
        static_cast<int64_t>(p.tp + 3) * 2 * p.H >= kDynamicMinRowBytes);
-  if (want_dynamic && p.rows_total + grid < (int64_t{1} << 31)) slot = counter_slot(dev, stream);
-  if (slot >= 0) {
+  if (want_dynamic && p.rows_total + grid < (int64_t{1} << 31)) {
+    // The caller's own counter, if given (its calls are ordered by the caller, even inside a
+    // captured graph); else this stream's slot of the library's table, if it has one.
+    if (x.row_counter) {
+      counter = static_cast<unsigned int*>(x.row_counter);
+    } else {
+      const int slot = counter_slot(dev, stream);
+      if (slot >= 0) counter = dev->counters + 2 * slot;
+    }
+  }
+  if (counter) {
     // The dynamic variant's own occupancy sizes its grid: every CTA must be resident from the
     // start, since each one begins with a fixed row.
     e = set_staged_smem_limit<kVec, kMode, true>(dev);
@@ -431,25 +460,35 @@ cudaError_t launch_one(const sp_launch_config& cfg, spk::Params& p, int smem, in
       e = persistent_grid(spk::k_staged<kVec, kMode, true>, threads, smem, cfg.ctas_per_sm,
                           p.T_pad, dev, &grid);
     if (e != cudaSuccess) return e;
-    p.counter_slot = slot;
-    e = launch_pdl(spk::k_staged<kVec, kMode, true>, grid, threads, smem, stream, p);
-  } else {
-    e = launch_pdl(spk::k_staged<kVec, kMode, false>, grid, threads, smem, stream, p);
+    p.row_counter = counter;
   }
+  void (*kernel)(spk::Params) =
+      counter ? spk::k_staged<kVec, kMode, true> : spk::k_staged<kVec, kMode, false>;
+  if constexpr (kVec == 2) {
+    if (x.withhold >= 0) {  // the self-test's instantiation (two vectors per thread only)
+      kernel = counter ? spk::k_staged<kVec, kMode, true, true>
+                       : spk::k_staged<kVec, kMode, false, true>;
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               kSmemPerCtaMax);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  e = launch_pdl(kernel, grid, threads, smem, stream, p);
+  t_last_launch.grid = grid;
+  t_last_launch.schedule = counter ? SP_SCHEDULE_DYNAMIC : SP_SCHEDULE_STATIC;
   return e != cudaSuccess ? e : cudaGetLastError();
 }
 
 template <int kVec>
 cudaError_t launch_mode(int mode, const sp_launch_config& cfg, spk::Params& p, int smem,
-                        int schedule, cudaStream_t stream, DeviceInfo* dev) {
+                        const Extras& x, cudaStream_t stream, DeviceInfo* dev) {
   switch (mode) {
-    case SP_QUANT_NONE:
-      return launch_one<kVec, spk::kModeNone>(cfg, p, smem, schedule, stream, dev);
+    case SP_QUANT_NONE: return launch_one<kVec, spk::kModeNone>(cfg, p, smem, x, stream, dev);
     case SP_QUANT_FP8_STATIC:
-      return launch_one<kVec, spk::kModeFp8Static>(cfg, p, smem, schedule, stream, dev);
+      return launch_one<kVec, spk::kModeFp8Static>(cfg, p, smem, x, stream, dev);
     case SP_QUANT_FP8_PER_TOKEN:
-      return launch_one<kVec, spk::kModeFp8PerToken>(cfg, p, smem, schedule, stream, dev);
-    default: return launch_one<kVec, spk::kModeNvfp4>(cfg, p, smem, schedule, stream, dev);
+      return launch_one<kVec, spk::kModeFp8PerToken>(cfg, p, smem, x, stream, dev);
+    default: return launch_one<kVec, spk::kModeNvfp4>(cfg, p, smem, x, stream, dev);
   }
 }
 
@@ -514,6 +553,9 @@ sp_status run_checked(const sp_launch_config& cfg_in, const void* partials, int 
     p.nthreads = split_threads(H, split_of(cfg), cfg.vec_per_thread);
   }
   p.eps = eps;
+  p.error_word = x.status ? x.status : dev->error_word;
+  p.wait_limit_ns = x.wait_limit_ns;
+  p.withhold = x.withhold;
   int smem = 0;
   if (cfg.kernel == SP_KERNEL_STAGED) {
     if (cfg.stages == 0) cfg.stages = max_stages(H, cfg.ctas_per_sm);
@@ -524,12 +566,19 @@ sp_status run_checked(const sp_launch_config& cfg_in, const void* partials, int 
     smem = p.ring_offset + p.stages * p.seg_stride;
   }
   cudaError_t e;
+  t_last_launch = sp_launch_info{};
+  t_last_launch.schedule = SP_SCHEDULE_STATIC;
   switch (cfg.vec_per_thread) {
-    case 1: e = launch_mode<1>(mode, cfg, p, smem, x.schedule, stream, dev); break;
-    case 2: e = launch_mode<2>(mode, cfg, p, smem, x.schedule, stream, dev); break;
-    default: e = launch_mode<4>(mode, cfg, p, smem, x.schedule, stream, dev); break;
+    case 1: e = launch_mode<1>(mode, cfg, p, smem, x, stream, dev); break;
+    case 2: e = launch_mode<2>(mode, cfg, p, smem, x, stream, dev); break;
+    default: e = launch_mode<4>(mode, cfg, p, smem, x, stream, dev); break;
   }
-  return e == cudaSuccess ? SP_OK : SP_ERR_CUDA;
+  if (e != cudaSuccess) {
+    t_last_launch = sp_launch_info{};
+    return SP_ERR_CUDA;
+  }
+  t_last_launch.config = cfg;
+  return SP_OK;
 }
 
 sp_status run(const sp_launch_config& cfg, const void* partials, int tp, int64_t T_pad,
@@ -736,21 +785,32 @@ void sp_options_init(sp_fused_options* options) {
   options->host_buffers = 0;
   options->schedule = SP_SCHEDULE_AUTO;
   options->launch = nullptr;
+  options->row_counter = nullptr;
+  options->status = nullptr;
 }
 
-sp_status sp_fused_reduce_norm_ex(const sp_fused_options* options, const void* partials, int tp,
-                                  int64_t T_pad, int64_t T_valid, int64_t H, const void* residual,
-                                  const void* weight, const void* bias, float eps, int quant_mode,
-                                  const float* scale, void* out, void* out_scales,
-                                  void* residual_out, sp_stream_t stream) {
-  sp_fused_options o;
-  sp_options_init(&o);
-  if (options) o = *options;
+}  // extern "C"
+
+namespace {
+
+Extras extras_of(const sp_fused_options& o) {
   Extras x;
   x.partial_scale = o.partial_scale;
   x.addend = o.addend;
   x.scale_layout = o.scale_layout;
   x.schedule = o.schedule;
+  x.row_counter = o.row_counter;
+  x.status = o.status;
+  return x;
+}
+
+// The checks of the options-taking entry points, in order: those of sp_fused_reduce_norm (with
+// the options' buffers), then host_buffers, then the forced launch.
+sp_status check_ex(const sp_fused_options& o, const Extras& x, const void* partials, int tp,
+                   int64_t T_pad, int64_t T_valid, int64_t H, const void* residual,
+                   const void* weight, const void* bias, float eps, int quant_mode,
+                   const float* scale, const void* out, const void* out_scales,
+                   const void* residual_out) {
   sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode,
                        scale, out, out_scales, residual_out, x);
   if (st != SP_OK) return st;
@@ -760,26 +820,48 @@ sp_status sp_fused_reduce_norm_ex(const sp_fused_options* options, const void* p
     if (st != SP_OK) return st;
     if (o.host_buffers && o.launch->kernel != SP_KERNEL_DIRECT) return SP_ERR_UNSUPPORTED;
   }
+  return SP_OK;
+}
+
+// sp_fused_reduce_norm_ex after its checks. staged_only: run the staged kernel whatever
+// sp_select_launch picks (the self-test of its abort path).
+sp_status run_ex(const sp_fused_options& o, Extras x, bool staged_only, const void* partials,
+                 int tp, int64_t T_pad, int64_t T_valid, int64_t H, const void* residual,
+                 const void* weight, const void* bias, float eps, int quant_mode,
+                 const float* scale, void* out, void* out_scales, void* residual_out,
+                 cudaStream_t s) {
   if (T_pad == 0) return SP_OK;
-  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   if (!o.host_buffers) {
     sp_launch_config cfg;
     if (o.launch) {
       cfg = *o.launch;
     } else {
-      st = sp_select_launch(tp, T_pad, H, quant_mode, &cfg);
+      const sp_status st = sp_select_launch(tp, T_pad, H, quant_mode, &cfg);
       if (st != SP_OK) return st;
     }
+    if (staged_only && cfg.kernel != SP_KERNEL_STAGED) {
+      if (o.launch) return SP_ERR_UNSUPPORTED;
+      cfg = sp_launch_config{};
+      cfg.kernel = SP_KERNEL_STAGED;
+      cfg.vec_per_thread = 2;
+      cfg.ctas_per_sm = 1;
+      cfg.stages = 0;
+      const sp_status st = config_is_valid(cfg, H);
+      if (st != SP_OK) return st;
+    }
+    // the self-test's kernel is built for two vectors per consumer thread (H <= 8192)
+    if (staged_only && cfg.vec_per_thread != 2) return SP_ERR_UNSUPPORTED;
     return run_checked(cfg, partials, tp, T_pad, T_valid, H, residual, weight, bias, eps,
                        quant_mode, scale, out, out_scales, residual_out, s, x);
   }
+  if (staged_only) return SP_ERR_UNSUPPORTED;
   // Host buffers: map every pointer to its device address and use plain 128-bit loads (the
   // direct kernel): the host link, not HBM, bounds this call, and a few hundred KB of loads in
   // flight per GPU cover its latency.
-  const void* host[9] = {partials, residual, weight, bias, scale, out, out_scales, residual_out,
-                         x.addend};
-  const void* dev[9];
-  for (int i = 0; i < 9; ++i)
+  const void* host[10] = {partials,     residual, weight,  bias, scale, out, out_scales,
+                          residual_out, x.addend, x.status};
+  const void* dev[10];
+  for (int i = 0; i < 10; ++i)
     if (!device_view(host[i], &dev[i])) return SP_ERR_INVALID_ARG;
   sp_launch_config cfg{};
   cfg.kernel = SP_KERNEL_DIRECT;
@@ -788,9 +870,31 @@ sp_status sp_fused_reduce_norm_ex(const sp_fused_options* options, const void* p
   cfg.stages = 0;
   if (o.launch) cfg = *o.launch;
   x.addend = dev[8];
+  x.status = static_cast<uint32_t*>(const_cast<void*>(dev[9]));
   return run(cfg, dev[0], tp, T_pad, T_valid, H, dev[1], dev[2], dev[3], eps, quant_mode,
              static_cast<const float*>(dev[4]), const_cast<void*>(dev[5]),
              const_cast<void*>(dev[6]), const_cast<void*>(dev[7]), s, x);
+}
+
+}  // namespace
+
+extern "C" {
+
+sp_status sp_fused_reduce_norm_ex(const sp_fused_options* options, const void* partials, int tp,
+                                  int64_t T_pad, int64_t T_valid, int64_t H, const void* residual,
+                                  const void* weight, const void* bias, float eps, int quant_mode,
+                                  const float* scale, void* out, void* out_scales,
+                                  void* residual_out, sp_stream_t stream) {
+  sp_fused_options o;
+  sp_options_init(&o);
+  if (options) o = *options;
+  const Extras x = extras_of(o);
+  const sp_status st = check_ex(o, x, partials, tp, T_pad, T_valid, H, residual, weight, bias,
+                                eps, quant_mode, scale, out, out_scales, residual_out);
+  if (st != SP_OK) return st;
+  return run_ex(o, x, false, partials, tp, T_pad, T_valid, H, residual, weight, bias, eps,
+                quant_mode, scale, out, out_scales, residual_out,
+                reinterpret_cast<cudaStream_t>(stream));
 }
 
 sp_status sp_fused_reduce_norm_host(const void* partials, int tp, int64_t T_pad, int64_t T_valid,
@@ -813,20 +917,34 @@ sp_status sp_check_args_ex(const sp_fused_options* options, const void* partials
   sp_fused_options o;
   sp_options_init(&o);
   if (options) o = *options;
-  Extras x;
-  x.partial_scale = o.partial_scale;
-  x.addend = o.addend;
-  x.scale_layout = o.scale_layout;
-  x.schedule = o.schedule;
-  sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode,
-                       scale, out, out_scales, residual_out, x);
+  return check_ex(o, extras_of(o), partials, tp, T_pad, T_valid, H, residual, weight, bias, eps,
+                  quant_mode, scale, out, out_scales, residual_out);
+}
+
+sp_status sp_selftest_fused_timeout(uint64_t limit_ns, int64_t withhold,
+                                    const sp_fused_options* options, const void* partials, int tp,
+                                    int64_t T_pad, int64_t T_valid, int64_t H,
+                                    const void* residual, const void* weight, const void* bias,
+                                    float eps, int quant_mode, const float* scale, void* out,
+                                    void* out_scales, void* residual_out, sp_stream_t stream) {
+  if (limit_ns == 0 || limit_ns > spk::kWaitLimitNs || withhold < 0) return SP_ERR_INVALID_ARG;
+  sp_fused_options o;
+  sp_options_init(&o);
+  if (options) o = *options;
+  Extras x = extras_of(o);
+  const sp_status st = check_ex(o, x, partials, tp, T_pad, T_valid, H, residual, weight, bias,
+                                eps, quant_mode, scale, out, out_scales, residual_out);
   if (st != SP_OK) return st;
-  if (o.host_buffers != 0 && o.host_buffers != 1) return SP_ERR_UNSUPPORTED;
-  if (o.launch) {
-    st = config_is_valid(*o.launch, H);
-    if (st != SP_OK) return st;
-    if (o.host_buffers && o.launch->kernel != SP_KERNEL_DIRECT) return SP_ERR_UNSUPPORTED;
-  }
+  x.wait_limit_ns = limit_ns;
+  x.withhold = withhold;
+  return run_ex(o, x, true, partials, tp, T_pad, T_valid, H, residual, weight, bias, eps,
+                quant_mode, scale, out, out_scales, residual_out,
+                reinterpret_cast<cudaStream_t>(stream));
+}
+
+sp_status sp_last_launch(sp_launch_info* info) {
+  if (!info) return SP_ERR_INVALID_ARG;
+  *info = t_last_launch;
   return SP_OK;
 }
 

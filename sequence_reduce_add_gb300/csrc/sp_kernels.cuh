@@ -32,16 +32,27 @@ namespace spk {
 constexpr int kMaxConsumerThreads = 512;  // 16 warps
 constexpr int kProducerThreads = 32;
 
-// Row counters of the dynamic schedule: slot i is [next claim, CTAs done]. A launch uses the slot
-// of its stream; its last CTA to finish claiming sets both words back to zero, so the next launch
-// on that stream (which starts claiming only after this one has completed) finds a zeroed slot.
+// Row counters of the dynamic schedule: slot i is [next claim, CTAs done]. A launch gets the
+// address of one pair (a slot of this table chosen by its stream, or a caller's own pair); its
+// last CTA to finish claiming sets both words back to zero, so the next launch using that pair
+// (which starts claiming only after this one has completed) finds it zeroed.
 constexpr int kRowCounterSlots = 256;
 __device__ unsigned int g_row_counters[2 * kRowCounterSlots];
 
+// The CTA's error word address, kept in shared memory beside the abort flag: a report site (a
+// cold path inside the row loops) reads it there instead of holding it in registers.
+__device__ __forceinline__ unsigned int* error_word_of(int* abort_flag) {
+  return *reinterpret_cast<unsigned int* volatile*>(abort_flag + 2);
+}
+
 // ----------------------------------------------------------------------------------- staged
-template <int kVec, int kMode, bool kDynamic>
+// kTest: the self-test instantiation (sp_selftest_fused_timeout): every bounded wait uses the
+// launch's p.wait_limit_ns and CTA 0's producer withholds ring fill number p.withhold. Production
+// instantiations use the fixed limit and withhold nothing.
+template <int kVec, int kMode, bool kDynamic, bool kTest = false>
 __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
     k_staged(const Params p) {
+  const uint64_t wait_limit = kTest ? p.wait_limit_ns : kWaitLimitNs;
   extern __shared__ __align__(128) unsigned char smem[];
   uint64_t* full = reinterpret_cast<uint64_t*>(smem);
   uint64_t* empty = full + p.stages;
@@ -67,6 +78,7 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
       mbar_init(smem_addr(empty + s), static_cast<uint32_t>(nc >> 5));
     }
     *abort_flag = 0;
+    *reinterpret_cast<unsigned int**>(abort_flag + 2) = p.error_word;
     fence_mbar_init();
   } else if (tid == nc) {
     // While the previous kernel of the stream may still be running, pull this CTA's first ring
@@ -86,6 +98,7 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
     // ------------------------------------------------------------ producer (one thread)
     if (tid != nc) return;
     const uint64_t policy = l2_evict_first_policy();
+    const int64_t withhold = (kTest && blockIdx.x == 0) ? p.withhold : -1;
     int stage = 0;
     uint32_t phase = 0;
     int64_t issued = 0;
@@ -94,9 +107,16 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
       for (int64_t t = blockIdx.x; t < p.T_valid && !aborted; t += gridDim.x) {
         for (int seg = 0; seg < nseg; ++seg) {
           const uint16_t* src = segment(t, seg);
-          if (!mbar_wait_bounded(smem_addr(empty + stage), phase ^ 1u, abort_flag)) {
-            if (!*static_cast<volatile int*>(abort_flag)) atomicOr(&g_error_flags, kErrWaitTimeout);
+          if (!mbar_wait_bounded(smem_addr(empty + stage), phase ^ 1u, abort_flag,
+                                 wait_limit)) {
+            if (!*static_cast<volatile int*>(abort_flag))
+            atomicOr(error_word_of(abort_flag), kErrWaitTimeout);
             *static_cast<volatile int*>(abort_flag) = 1;
+            aborted = true;
+            break;
+          }
+          if (kTest && issued == withhold) {  // this stage never fills; issue nothing more
+            ++issued;
             aborted = true;
             break;
           }
@@ -113,20 +133,27 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
     } else {
       // Every row, padding rows included, takes one ring stage for its index (a padding row and
       // the final -1 take it alone: the producer completes that stage's phase by arriving).
-      unsigned int* counter = g_row_counters + 2 * p.counter_slot;
+      unsigned int* counter = p.row_counter;
       int64_t next = blockIdx.x;
       for (;;) {
         const int64_t t = next < p.rows_total ? next : -1;
         if (t >= 0) next = static_cast<int64_t>(gridDim.x) + atomicAdd(counter, 1u);
         for (int seg = 0; seg < (t >= 0 && t < p.T_valid ? nseg : 1); ++seg) {
-          if (!mbar_wait_bounded(smem_addr(empty + stage), phase ^ 1u, abort_flag)) {
-            if (!*static_cast<volatile int*>(abort_flag)) atomicOr(&g_error_flags, kErrWaitTimeout);
+          if (!mbar_wait_bounded(smem_addr(empty + stage), phase ^ 1u, abort_flag,
+                                 wait_limit)) {
+            if (!*static_cast<volatile int*>(abort_flag))
+            atomicOr(error_word_of(abort_flag), kErrWaitTimeout);
             *static_cast<volatile int*>(abort_flag) = 1;
             aborted = true;
             break;
           }
           const uint32_t bar = smem_addr(full + stage);
           if (seg == 0) row_ids[stage] = t;
+          if (kTest && issued == withhold) {  // this stage never fills; issue nothing more
+            ++issued;
+            aborted = true;
+            break;
+          }
           if (t >= 0 && t < p.T_valid) {
             mbar_arrive_expect_tx(bar, seg_bytes);
             bulk_g2s(smem_addr(ring + stage * p.seg_stride), segment(t, seg), seg_bytes, bar,
@@ -149,12 +176,12 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
     for (int64_t s = 0; s < used; ++s) {
       const int64_t last = issued - 1 - ((issued - 1 - s) % p.stages);  // last issue on stage s
       const uint32_t par = static_cast<uint32_t>((last / p.stages) & 1);
-      if (!mbar_wait_bounded(smem_addr(full + s), par, nullptr))
-        atomicOr(&g_error_flags, kErrWaitTimeout);
+      if (!mbar_wait_bounded(smem_addr(full + s), par, nullptr, wait_limit))
+        atomicOr(error_word_of(abort_flag), kErrWaitTimeout);
     }
     if constexpr (kDynamic) {
-      // This CTA claims no more rows; the last CTA of the launch to get here resets the slot.
-      unsigned int* counter = g_row_counters + 2 * p.counter_slot;
+      // This CTA claims no more rows; the last CTA of the launch to get here resets the pair.
+      unsigned int* counter = p.row_counter;
       __threadfence();
       if (atomicAdd(counter + 1, 1u) == gridDim.x - 1) {
         counter[0] = 0u;
@@ -198,13 +225,20 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
         continue;
       }
     } else {
-      // The row's index sits beside its first stage. A warp acts on the wait only as a whole; a
-      // warp whose wait ran out still passes the row barrier (voting to stop), so all consumer
-      // warps pass the same barriers.
-      const bool landed = mbar_wait_bounded(smem_addr(full + stage), phase, abort_flag);
+      // The row's index sits beside its first stage. A warp acts on the wait only as a whole.
+      // Every warp leaves the loop through exactly one row barrier after the last one all warps
+      // passed together: the abort vote here (a warp whose wait ran out), the bare barrier below
+      // (no more rows), or a row's own barrier in finish_row. All warps read the same row
+      // indices, so whatever mix of these the warps take, each takes one; warps at a row's
+      // barrier then read the abort vote and leave too. (Leaving without a barrier on "no more
+      // rows" could strand a sibling warp in its abort vote if its wait ran out just as the
+      // stage completed.)
+      const bool landed =
+          mbar_wait_bounded(smem_addr(full + stage), phase, abort_flag, wait_limit);
       if (!__all_sync(0xFFFFFFFFu, landed)) {
         if (lane == 0) {
-          if (!*static_cast<volatile int*>(abort_flag)) atomicOr(&g_error_flags, kErrWaitTimeout);
+          if (!*static_cast<volatile int*>(abort_flag))
+            atomicOr(error_word_of(abort_flag), kErrWaitTimeout);
           *static_cast<volatile int*>(abort_flag) = 1;
         }
         int ignored = 0;
@@ -212,7 +246,10 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
         break;
       }
       t = row_ids[stage];
-      if (t < 0) break;
+      if (t < 0) {
+        named_barrier_sync(1, nc);
+        break;
+      }
       if (t >= p.T_valid) {
         __syncwarp();
         if (lane == 0) mbar_arrive(smem_addr(empty + stage));
@@ -238,8 +275,10 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
 
     int aborted = 0;
     for (int seg = 0; seg < nseg; ++seg) {
-      if (!aborted && !mbar_wait_bounded(smem_addr(full + stage), phase, abort_flag)) {
-        if (!*static_cast<volatile int*>(abort_flag)) atomicOr(&g_error_flags, kErrWaitTimeout);
+      if (!aborted &&
+          !mbar_wait_bounded(smem_addr(full + stage), phase, abort_flag, wait_limit)) {
+        if (!*static_cast<volatile int*>(abort_flag))
+          atomicOr(error_word_of(abort_flag), kErrWaitTimeout);
         *static_cast<volatile int*>(abort_flag) = 1;
         aborted = 1;
       }
@@ -274,6 +313,9 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
     parity ^= 1;
     if (stop) break;  // every consumer sees the same vote, so all leave together
   }
+  // A consumer whose wait ran out set the abort flag before the row barrier that every
+  // consumer passed on the way out, so thread 0 sees it here and reports it once for the CTA.
+
 }
 
 // ----------------------------------------------------------------------------------- direct

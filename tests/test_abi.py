@@ -295,6 +295,14 @@ OPTION_CASES = [
     (dict(launch=dict(kernel=1, vec_per_thread=2, ctas_per_sm=4), host_buffers=1), {}, "SP_OK"),
     (dict(launch=dict(kernel=0, vec_per_thread=2, ctas_per_sm=2, stages=3), host_buffers=1), {},
      "SP_ERR_UNSUPPORTED"),
+    # the caller's row counter (8 bytes) and status word (4 bytes): aligned, overlapping nothing
+    (dict(row_counter=A * 21, status=A * 22), {}, "SP_OK"),
+    (dict(row_counter=A * 21 + 8), {}, "SP_ERR_ALIGNMENT"),
+    (dict(status=A * 22 + 4), {}, "SP_ERR_ALIGNMENT"),
+    (dict(row_counter=A * 11), {}, "SP_ERR_INVALID_ARG"),           # inside `out`
+    (dict(status=A * 8 + 16), {}, "SP_ERR_INVALID_ARG"),            # inside the residual
+    (dict(row_counter=A * 21, status=A * 21), {}, "SP_ERR_INVALID_ARG"),  # the same bytes
+    (dict(status=A * 9), {}, "SP_ERR_INVALID_ARG"),                 # is the weight
 ]
 
 
@@ -305,6 +313,7 @@ def test_option_checks(lib, opt, kw, want):
     assert o.partial_scale == 1.0 and o.addend is None and o.scale_layout == 0
     assert o.host_buffers == 0 and o.schedule == 0  # SP_SCHEDULE_AUTO
     assert not o.launch  # NULL: the library's own choice
+    assert o.row_counter is None and o.status is None
     cfg = None
     for k, v in opt.items():
         if k == "launch":

@@ -390,7 +390,21 @@ def test_dynamic_schedule_on_two_streams_concurrently():
 
 
 def test_dynamic_schedule_with_more_streams_than_counter_slots():
-    """Streams beyond the counter table fall back to the static schedule: still correct."""
+    """Streams beyond the counter table fall back to the static schedule: still correct. Runs in a
+    child process, so that this process's table keeps free slots for the other tests."""
+    import os
+    import subprocess
+    import sys
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, PYTHONPATH=os.pathsep.join(
+        [os.path.dirname(here), here, os.environ.get("PYTHONPATH", "")]))
+    proc = subprocess.run([sys.executable, os.path.abspath(__file__), "streams"], cwd=here,
+                          env=env, capture_output=True, text=True, timeout=600)
+    assert proc.returncode == 0, proc.stdout[-2000:] + proc.stderr[-2000:]
+    assert "streams ok" in proc.stdout
+
+
+def _more_streams_than_counter_slots():
     w = synth.workload(2)
     inp = _small(w, rows=64)
     outs = [sp.allocate_outputs(inp["T_pad"], inp["H"], inp["mode"], DEV) for _ in range(300)]
@@ -410,6 +424,7 @@ def test_dynamic_schedule_with_more_streams_than_counter_slots():
             assert np.array_equal(h[k].view(np.uint8), first[k].view(np.uint8))
     for st in raw:
         _destroy_raw_stream(st.cuda_stream)
+    print("streams ok")
 
 
 def _cudart():
@@ -792,3 +807,9 @@ def test_split_rows_captured_in_a_graph_after_other_kernels():
     torch.cuda.synchronize()
     fresh["partials"] = (fresh["partials"].float() * 0.5).to(torch.bfloat16)
     compare(_host(outs), run_oracle(fresh), fresh)
+
+
+if __name__ == "__main__":
+    import sys
+    if sys.argv[1:] == ["streams"]:
+        _more_streams_than_counter_slots()
