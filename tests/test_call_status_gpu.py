@@ -172,6 +172,7 @@ def _streams_beyond_the_table():
     try:
         small = _small(synth.workload(3), rows=16)
         so = sp.allocate_outputs(small["T_pad"], small["H"], small["mode"], DEV)
+        torch.cuda.synchronize()  # inputs written on torch's stream before the raw streams read
         staged = dict(kernel=0, vec_per_thread=2, ctas_per_sm=2, stages=0)
         for h in handles:  # one dynamic staged call per stream takes (or finds) its slot
             _call(small, so, sp.sp_options_init(schedule="dynamic", launch=staged), stream=h)
@@ -206,6 +207,7 @@ def test_caller_row_counter_inside_a_captured_graph():
     counter = _words(4)
     s = torch.cuda.Stream(device=DEV)
     opts = sp.sp_options_init(schedule="dynamic", row_counter=counter)
+    torch.cuda.synchronize()  # inputs written on torch's stream before `s` reads them
     with torch.cuda.stream(s):
         _call(inp, outs, opts)  # warm-up outside the capture
     torch.cuda.synchronize()

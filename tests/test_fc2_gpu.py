@@ -66,6 +66,7 @@ def test_fc2_reads_what_the_fused_stage_just_wrote():
     out = torch.empty_like(res_out)
     y = torch.empty((G, N // D, D * F), dtype=torch.bfloat16, device=DEV)
     s = torch.cuda.Stream(device=DEV)
+    torch.cuda.synchronize()  # the inputs are written on torch's stream; `s` does not wait for it
 
     def step():
         sp.sp_fused_reduce_norm(inp["partials"], inp["weight"], out, res_out,
@@ -80,6 +81,7 @@ def test_fc2_reads_what_the_fused_stage_just_wrote():
 
     for k in range(5):
         inp["partials"].mul_(0.5 if k % 2 else 2.0)   # new contents every step
+        torch.cuda.current_stream().synchronize()
         step()
         check()
     g = torch.cuda.CUDAGraph()

@@ -133,6 +133,7 @@ def test_side_stream():
     w = synth.workload(2)
     inp = _small(w)
     s = torch.cuda.Stream(device=DEV)
+    torch.cuda.synchronize()  # the inputs are written on torch's stream; `s` does not wait for it
     with torch.cuda.stream(s):
         _check(inp, stream=s)
 
@@ -292,6 +293,7 @@ def test_cuda_graph_capture_and_replay(wi):
                                 quant_mode=inp["mode"], scale=scale,
                                 out_scales=outs["out_scales"], T_valid=inp["T_valid"])
 
+    torch.cuda.synchronize()  # the inputs are written on torch's stream; `s` does not wait for it
     with torch.cuda.stream(s):
         call()
     torch.cuda.synchronize()
@@ -781,6 +783,7 @@ def test_split_rows_captured_in_a_graph_after_other_kernels():
     src = inp["partials"].clone()
     opts = sp.sp_options_init(launch=_split_cfg(8, 1))
     s = torch.cuda.Stream(device=DEV)
+    torch.cuda.synchronize()  # the inputs are written on torch's stream; `s` does not wait for it
 
     def step():
         inp["partials"].copy_(src)
