@@ -253,6 +253,36 @@ sp_status sp_fused_reduce_norm_host(const void* partials, int tp, int64_t T_pad,
                                     void* residual_out, sp_stream_t stream);
 
 /*
+ * sp_fused_reduce_norm_noalloc — sp_fused_reduce_norm for callers that may not allocate device
+ * memory. Some code cannot call cudaMalloc or any allocating routine at the point where it runs
+ * this stage: code recording a CUDA graph (allocation is not a capturable operation), a plugin
+ * or custom operator whose host framework owns every device buffer and hands out only the
+ * tensors of the call, and latency-critical serving loops that forbid allocation after start-up
+ * (cudaMalloc can synchronise the device and take milliseconds). Such a caller cannot provide
+ * the 8-byte row counter that the dynamic row schedule needs (sp_fused_options.row_counter), and
+ * the library's per-stream counter table serves only the first 256 streams of a process. This
+ * entry point keeps that counter in an array of the library's own static device memory instead:
+ * 8 bytes, one array per GPU that loads the library, held until the process exits, shared by
+ * every call of this entry point. The caller passes exactly the buffers of sp_fused_reduce_norm.
+ *
+ * Same arguments, checks, statuses, launch choice and results (byte for byte) as
+ * sp_fused_reduce_norm; nothing is allocated, by the library or on its behalf. Before its launch
+ * it clears the counter on `stream` (cudaMemsetAsync of the 8 bytes), since the array keeps what
+ * the previous call left. The first call on a device looks up the array's device address with
+ * cudaGetSymbolAddress; make that first call before any stream capture on that device. Calls of
+ * this entry point that overlap on the GPU (on different streams, or in graph replays that run at
+ * the same time) share the one counter and race: order them, for instance on one stream.
+ * Maximum: T_pad up to 2^31 - 2^16 rows, the range of the 32-bit counter; larger calls return
+ * SP_ERR_UNSUPPORTED before anything is enqueued. The pages have no counterpart of this entry
+ * point (it concerns memory management only): no counterpart on the pages.
+ */
+sp_status sp_fused_reduce_norm_noalloc(const void* partials, int tp, int64_t T_pad,
+                                       int64_t T_valid, int64_t H, const void* residual,
+                                       const void* weight, const void* bias, float eps,
+                                       int quant_mode, const float* scale, void* out,
+                                       void* out_scales, void* residual_out, sp_stream_t stream);
+
+/*
  * Launch configurations. sp_fused_reduce_norm picks one by itself (sp_select_launch tells
  * which); sp_fused_reduce_norm_with_config runs a given one, for tests and tuning. Every
  * configuration computes the same function.

@@ -25,7 +25,7 @@ __all__ = [
     "sp_device_error", "allocate_outputs", "LaunchConfig", "Options", "sp_options_init",
     "sp_fused_reduce_norm_ex", "sp_check_args_ex", "sp_out_scales_bytes_ex", "sp_fc2_reorganize",
     "sp_fc2_check_args", "sp_fc2_batch_ids", "sp_selftest_wait_timeout",
-    "sp_selftest_fused_timeout", "sp_last_launch", "LaunchInfo",
+    "sp_selftest_fused_timeout", "sp_last_launch", "LaunchInfo", "sp_fused_reduce_norm_noalloc",
 ]
 
 QUANT_MODES = {"none": 0, "fp8_static": 1, "fp8_per_token": 2, "nvfp4": 3,
@@ -143,6 +143,8 @@ def load_library() -> ctypes.CDLL:
     lib.sp_selftest_fused_timeout.restype = ctypes.c_int
     lib.sp_last_launch.argtypes = [ctypes.POINTER(LaunchInfo)]
     lib.sp_last_launch.restype = ctypes.c_int
+    lib.sp_fused_reduce_norm_noalloc.argtypes = _MAIN_ARGS + [_vp]
+    lib.sp_fused_reduce_norm_noalloc.restype = ctypes.c_int
     _lib = lib
     return lib
 
@@ -253,6 +255,21 @@ def sp_fused_reduce_norm(partials, weight, out, residual_out, *, residual=None, 
     st = load_library().sp_fused_reduce_norm(*args, _stream_handle(stream))
     if st != 0:
         raise SpError(st, "sp_fused_reduce_norm")
+
+
+def sp_fused_reduce_norm_noalloc(partials, weight, out, residual_out, *, residual=None,
+                                 bias=None, eps: float = 1e-6, quant_mode="none", scale=None,
+                                 out_scales=None, T_valid: int | None = None,
+                                 stream=None) -> None:
+    """``sp_fused_reduce_norm`` for callers that may not allocate device memory (inside a graph
+    capture, in a framework that owns every buffer, in an allocation-free serving loop): the
+    dynamic row schedule's counter lives in the library's own static device memory. Calls that
+    overlap on the GPU share that counter: order them (see include/sp_fused.h)."""
+    args = _main_args(partials, residual, weight, bias, eps, quant_mode, scale, out, out_scales,
+                      residual_out, T_valid)
+    st = load_library().sp_fused_reduce_norm_noalloc(*args, _stream_handle(stream))
+    if st != 0:
+        raise SpError(st, "sp_fused_reduce_norm_noalloc")
 
 
 def sp_options_init(*, partial_scale: float = 1.0, addend=None, scale_layout: int = 0,

@@ -1096,3 +1096,75 @@ sp_status sp_device_error(uint32_t* flags, int clear) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------ entry point that allocates nothing
+// sp_fused_reduce_norm_noalloc keeps the dynamic row schedule's scratch (its row counter pair) in
+// this file's own static device array instead of a per-stream slot or a caller's buffer, so a
+// caller that may not allocate device memory still gets that schedule on any stream. The array
+// exists once per GPU that loads the library and lives until the process exits.
+namespace {
+
+constexpr int kNoAllocScratchWords = 2;  // [next claim, CTAs done]: 8 bytes
+// The row counter counts rows with 32-bit atomics on top of the grid; calls with more rows than
+// this are refused rather than run with a counter that could wrap.
+constexpr int64_t kNoAllocMaxRows = (int64_t{1} << 31) - (int64_t{1} << 16);
+
+static __device__ __align__(256) unsigned int g_noalloc_scratch[kNoAllocScratchWords];
+
+// Device address of g_noalloc_scratch in each device's context, looked up on the first call made
+// on that device (with it current). In host code the array's name is only a stand-in for the
+// symbol, never a pointer a kernel may be given.
+std::atomic<unsigned int*> g_noalloc_scratch_addr[kMaxDevices];
+std::mutex g_noalloc_mutex;
+
+sp_status noalloc_scratch(unsigned int** addr) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return SP_ERR_CUDA;
+  unsigned int* p = g_noalloc_scratch_addr[dev].load(std::memory_order_acquire);
+  if (!p) {
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    p = g_noalloc_scratch_addr[dev].load(std::memory_order_relaxed);
+    if (!p) {
+      void* sym = nullptr;
+      if (cudaGetSymbolAddress(&sym, g_noalloc_scratch) != cudaSuccess || !sym)
+        return SP_ERR_CUDA;
+      p = static_cast<unsigned int*>(sym);
+      g_noalloc_scratch_addr[dev].store(p, std::memory_order_release);
+    }
+  }
+  *addr = p;
+  return SP_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+sp_status sp_fused_reduce_norm_noalloc(const void* partials, int tp, int64_t T_pad,
+                                       int64_t T_valid, int64_t H, const void* residual,
+                                       const void* weight, const void* bias, float eps,
+                                       int quant_mode, const float* scale, void* out,
+                                       void* out_scales, void* residual_out,
+                                       sp_stream_t stream) {
+  sp_status st = check(partials, tp, T_pad, T_valid, H, residual, weight, bias, eps, quant_mode,
+                       scale, out, out_scales, residual_out);
+  if (st != SP_OK) return st;
+  if (T_pad > kNoAllocMaxRows) return SP_ERR_UNSUPPORTED;
+  if (T_pad == 0) return SP_OK;
+  unsigned int* scratch = nullptr;
+  st = noalloc_scratch(&scratch);
+  if (st != SP_OK) return st;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  // The array keeps whatever the previous call left: the counter must start at zero.
+  if (cudaMemsetAsync(scratch, 0, kNoAllocScratchWords * sizeof(unsigned int), s) != cudaSuccess)
+    return SP_ERR_CUDA;
+  sp_launch_config cfg;
+  st = sp_select_launch(tp, T_pad, H, quant_mode, &cfg);
+  if (st != SP_OK) return st;
+  Extras x;
+  x.row_counter = scratch;
+  return run_checked(cfg, partials, tp, T_pad, T_valid, H, residual, weight, bias, eps,
+                     quant_mode, scale, out, out_scales, residual_out, s, x);
+}
+
+}  // extern "C"
