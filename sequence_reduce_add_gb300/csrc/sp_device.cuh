@@ -338,32 +338,49 @@ __device__ __forceinline__ int cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return static_cast<int>(r);
 }
-// Every thread of every CTA of the cluster: writes before it are seen by reads after it.
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
-               ::: "memory");
+// The cluster barrier in two halves: every thread of every CTA arrives (its earlier writes,
+// shared-memory writes to other CTAs included, are released), and a thread's wait returns once
+// all threads of the cluster have arrived. A thread waits before it arrives again.
+__device__ __forceinline__ void cluster_arrive() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
 }
-// Two floats from CTA `rank`'s copy of this CTA's shared-memory address `addr`.
-__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t addr, int rank) {
+__device__ __forceinline__ void cluster_wait() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+// Two floats into CTA `rank`'s copy of this CTA's shared-memory address `addr`.
+__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, int rank, float2 v) {
   uint32_t remote;
-  float2 v;
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
-  asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(remote)
+  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(v.x), "f"(v.y)
                : "memory");
-  return v;
 }
-// Split rows: the CTA-wide (sum of squares, max) of each CTA of the cluster, combined in rank
-// order (the same sum in every CTA). cslots: two slots in this CTA's shared memory, used on
-// alternate rows, so one cluster barrier per row suffices.
+// Split rows: the exchange of each row's (sum of squares, max) between the CTAs of a cluster.
+// Threads 0 .. kSplit-1 push the CTA-wide pair into slot [row parity][own rank] of every CTA of
+// the cluster (one peer each), a cluster barrier makes the pushes visible, and each CTA adds the
+// kSplit pairs from its own shared memory in rank order, so every CTA gets the same bits. Slots
+// alternate between rows: a CTA pushes into slot p again two rows later, after the barrier of
+// the row in between, which every CTA reaches only after reading slot p. The first exchange
+// first waits on the set-up barrier every CTA arrived at when it started (no CTA writes into a
+// peer that is not yet running); nothing is accessed in a peer after the last row's barrier, so
+// a CTA may exit right after it. The barriers are the hardware cluster barrier: every CTA of the
+// cluster walks the same rows, so all take the same barriers, and no wait here can time out.
+__shared__ float2 g_xslots[2][8];  // this CTA's [row parity][source rank] pairs
+
 template <int kSplit>
-__device__ __forceinline__ float2 cluster_row_sum(float2 part, float2* cslots, int parity) {
-  if (threadIdx.x == 0) cslots[parity] = part;
-  cluster_sync();
-  const uint32_t addr = smem_addr(cslots + parity);
+__device__ __forceinline__ float2 cluster_row_sum(float2 part, int rank, int parity,
+                                                  bool& setup_seen) {
+  if (!setup_seen) {
+    cluster_wait();
+    setup_seen = true;
+  }
+  if (threadIdx.x < kSplit)
+    st_cluster_f32x2(smem_addr(&g_xslots[parity][rank]), static_cast<int>(threadIdx.x), part);
+  cluster_arrive();
+  cluster_wait();
   float ss = 0.0f, mx = 0.0f;
 #pragma unroll
   for (int r = 0; r < kSplit; ++r) {
-    const float2 v = ld_cluster_f32x2(addr, r);
+    const float2 v = g_xslots[parity][r];
     ss += v.x;
     mx = fmaxf(mx, v.y);
   }
@@ -484,20 +501,20 @@ __device__ __forceinline__ void zero_row(const Params& p, int64_t t, int c, int 
 
 // Finish row t: h holds sum_r partials + residual + bias for this thread's vectors (zero for
 // vectors past the row). Writes residual_out, normalises, quantises and stores. Returns the
-// CTA-wide abort vote. Split rows (kSplit > 1): this CTA owns vectors [vbase, vend) and the row's
-// sums are combined across the cluster through cslots.
+// CTA-wide abort vote. Split rows (kSplit > 1): this CTA (cluster rank `rank`) owns vectors
+// [vbase, vend) and the row's sums are combined across the cluster by cluster_row_sum.
 template <int kVec, int kMode, int kSplit = 1>
 __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)[kVec][8],
                                           const uint4 (&w)[kVec], const QuantConst& qc,
                                           RedSlot* slots, int parity, int c, int abort,
-                                          int vbase = 0, int vend = 0,
-                                          float2* cslots = nullptr) {
+                                          int vbase = 0, int vend = 0, int rank = 0,
+                                          bool* setup_seen = nullptr) {
   const int64_t H = p.H;
   const int v0 = kSplit > 1 ? vbase : 0;
   const int vlim = kSplit > 1 ? vend : p.nvec;
   float ss0 = 0.0f, ss1 = 0.0f;  // sums of squares of the even and the odd elements
-  // Split rows: the new residual is stored after the cluster barrier, whose release would
-  // otherwise wait for these stores to complete.
+  // Split rows: the new residual is stored after the exchange, whose release would otherwise
+  // wait for these stores to complete.
   uint4 res[kSplit > 1 ? kVec : 1];
 #pragma unroll
   for (int k = 0; k < kVec; ++k) {
@@ -526,7 +543,7 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
   float2 red =
       row_reduce<kMode == kModeFp8PerToken>(ss, mx, abort, slots, parity, p.nthreads, &abort_all);
   if constexpr (kSplit > 1) {
-    red = cluster_row_sum<kSplit>(red, cslots, parity);
+    red = cluster_row_sum<kSplit>(red, rank, parity, *setup_seen);
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
       const int v = v0 + c + k * p.nthreads;

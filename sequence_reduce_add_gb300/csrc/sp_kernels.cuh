@@ -330,13 +330,15 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
   static_assert(kBatch == 4 || (kBatch == 8 && kVec == 1), "batch of 4, or 8 at one vector");
   constexpr bool kEarlyResidual = kVec <= 2;  // residual row loaded before the partials
   __shared__ RedSlot slots[64];
-  __shared__ float2 cslots[2];
   const int c = threadIdx.x;
   const int nc = p.nthreads;
   const int64_t H = p.H;
-  const int vbase = kSplit > 1 ? cluster_rank() * p.split_chunk : 0;
+  const int rank = kSplit > 1 ? cluster_rank() : 0;
+  const int vbase = kSplit > 1 ? rank * p.split_chunk : 0;
   const int vend = kSplit > 1 ? min(vbase + p.split_chunk, p.nvec) : p.nvec;
   const int vc = vbase + c;  // this thread's first vector
+  bool setup_seen = false;  // split rows: waited on the set-up cluster barrier
+  if constexpr (kSplit > 1) cluster_arrive();  // the set-up barrier (cluster_row_sum)
   pdl_launch_dependents();
   pdl_wait_prerequisites();
   uint4 w[kVec], b[kVec];
@@ -433,11 +435,14 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
     }
 #pragma unroll
     for (int k = 0; k < kVec; ++k) add_bf16x8(b[k], h[k]);
-    finish_row<kVec, kMode, kSplit>(p, t, h, w, qc, slots, parity, c, 0, vbase, vend, cslots);
+    finish_row<kVec, kMode, kSplit>(p, t, h, w, qc, slots, parity, c, 0, vbase, vend, rank,
+                                    &setup_seen);
     parity ^= 1;
   }
-  // No CTA leaves while another CTA of its cluster may still read its cslots.
-  if constexpr (kSplit > 1) cluster_sync();
+  // A CTA that made no exchange still completes the set-up barrier it arrived at.
+  if constexpr (kSplit > 1) {
+    if (!setup_seen) cluster_wait();
+  }
 }
 
 // ----------------------------------------------------------------------------------- self-test
