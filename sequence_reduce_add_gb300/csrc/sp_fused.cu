@@ -624,91 +624,104 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     c.kernel = SP_KERNEL_DIRECT;
     c.stages = 0;
   }
-  // Small calls (decode-sized batches) are latency-bound, every CTA doing about one row. The
-  // direct kernel (no ring to set up; loads four or eight partials at a time) is fastest while
-  // its loads fit in one wave; the staged kernel's floor grows with the row's segment count
-  // (each passes through the ring in turn), but it keeps all of a row's segments in flight with a
-  // deep ring.
-  // With only a few rows, one SM per row caps the call at what an SM can pull in (about
-  // 45 GB/s): splitting each row across a cluster of 2, 4 or 8 CTAs draws on that many more SMs.
-  // From GB300 sweeps of tp 2-16, H 1024-16384, T 1-4096 (call time, launches replayed from a
-  // CUDA graph and single launches):
-  //   H <= 4096, tp <= 5, T <= 256: direct below ~1.5M partial elements for tp <= 4 (2M for
-  //                        tp = 5), else the staged kernel at 2 CTAs/SM with as many stages as
-  //                        fit (7-27 % faster than either previous choice);
-  //   H <= 4096 otherwise: direct while T * H <= 2^20 (2^22 for H <= 1024, where a row's 2 KB
-  //                        segments leave the ring little to hide: 10-35 % faster; at tp >= 8
-  //                        and T <= 256, 13-70 % faster than the deep ring);
-  //   4096 < H <= 8192:    split rows (one vector per thread) for few rows: tp >= 12, 8 CTAs
-  //                        per row up to 16 rows and 4 up to 64 (10-100 % faster); 6 <= tp < 12,
-  //                        8 up to 8 rows, 4 up to 32 and 2 up to 64 (5-35 %); tp 2-5 at
-  //                        H >= 7168, 8 up to 8 rows (0-10 %); split rows lost at H <= 4096.
-  //                        Otherwise direct while tp * T * H <= 2^20 (13-30 % faster at T = 8-64)
-  //                        or, for tp >= 12, up to 128 rows (0-29 %); for 64-128 rows, the staged
-  //                        kernel at one CTA per SM with every stage that fits (a 12-stage ring
-  //                        at H = 8192: 10-34 % faster);
-  //   H > 8192:            split rows, one vector per thread: 8 CTAs per row up to 64 rows for
-  //                        tp >= 12; 8 up to 32 and 4 up to 64 for 6 <= tp < 12; 8 up to 16 and
-  //                        (tp >= 3) 4 up to 32 for tp 2-5 (2-85 % faster); else direct (four
-  //                        vectors per thread) up to 32 rows (7-35 % faster than the staged
-  //                        kernel; at 64 rows it was 3-11 % slower);
-  //   4096 < H <= 6144, more rows than SMs but no more than one round of the large-call grid:
-  //                        ceil(T / SMs) CTAs per SM, every stage that fits (6-27 % faster at
-  //                        T = 160-456; at H = 4096 and from 7168 up it was a wash);
-  //   H >= 4096, between one and two rounds of the large-call grid: the CTAs per SM whose last
-  //                        round is fullest, every stage that fits (5-21 % faster at H = 4096
-  //                        and 5120, T = 512-896).
+  // Calls with few rows (decode-sized batches up to a few hundred tokens) are latency-bound:
+  // every CTA does about one row, so the call time is one round trip per batch of loads plus the
+  // epilogue. The direct kernel (no ring to set up; loads four or eight partial rows at a time)
+  // wins while its loads fit in about one wave; with only a few long rows, splitting each row
+  // across a cluster of 2, 4 or 8 CTAs draws on that many more SMs (one SM pulls in about
+  // 45 GB/s); past that the staged kernel, with one round of rows given the deepest ring that
+  // fits (ceil(T / SMs) CTAs per SM), or the large-call rule below. From GB300 sweeps of tp 2-16,
+  // H 1024-16384, T 8-512, bf16 and per-token FP8 output, each launch timed back to back and
+  // replayed from a CUDA graph (inputs L2-resident, as the output of the kernel before them
+  // would be); against the previous rule this choice is 4.3 % faster summed over the 1186 swept
+  // shapes and within 0.8 % of the best measured launch of each:
+  //   H <= 4096:        direct while T * H <= 2^20 (tp >= 12 from H = 3072: and tp * T * H <=
+  //                     12.6 M), or, except for NVFP4 output, T * H <= 1.4 M at tp <= 4 (1.2 M at
+  //                     tp <= 8); two vectors per thread at tp <= 4 and 2^18 <= T * H <= 800 K
+  //                     (not for NVFP4; up to 27 % faster than the deep ring this replaced at
+  //                     tp <= 5); else, for H >= 3072 and at most four rounds of 152 rows,
+  //                     ceil(T / 152) CTAs per SM with every stage that fits (15-40 % faster at
+  //                     T = 320-448);
+  //   4096 < H <= 8192: split rows: 2 <= tp <= 5 and H >= 6144, 8 CTAs per row up to 16 rows;
+  //                     6 <= tp < 12, 8 up to 12 rows and 4 up to 64 (at H = 5120, 4 up to 32
+  //                     and 2 up to 64); tp >= 12, 8 up to 16 rows (4 below H = 7168) and 4 up
+  //                     to 64. Then direct with two vectors per thread up to 128 rows (160 at
+  //                     tp <= 3 and H >= 7168; at tp >= 12 up to 96, or 128 below H = 8192:
+  //                     15-36 % faster than the one-CTA-per-SM deep ring it replaced), split 2 up
+  //                     to 224 rows at H = 5120 and split 4 up to 160 at H = 6144 (tp < 12); the
+  //                     deep ring at one CTA per SM for tp >= 12 and 97-128 rows at H = 8192; one
+  //                     round of rows for H <= 6144 (17-41 % faster at H = 6144, T = 320-384);
+  //   H > 8192:         split rows (tp >= 2): 8 CTAs per row up to 16 rows (24 at tp >= 6), 4 up
+  //                     to 64, 8 up to 80 at H <= 12288 (16-36 % faster); then at tp <= 5 direct
+  //                     with four vectors per thread up to 96 rows (128 at H <= 12288); else
+  //                     staged.
   const int64_t elems = static_cast<int64_t>(tp) * T_pad * H;
+  const int64_t rows_x_h = T_pad * H;
   bool direct = false;
-  bool deep_ring = false;
-  bool deep_ring_1 = false;
+  bool ring_1 = false;  // staged at one CTA per SM with the deepest ring
+  int one_round = 0;    // staged at this many CTAs per SM with the deepest ring
+  int vec = 0;          // direct kernel: vectors per thread (0: by H)
   int split = 0;
+  const bool nvfp4 = quant_mode == SP_QUANT_NVFP4;
   if (H <= 4096) {
-    if (T_pad <= 256 && tp <= 5) {
-      direct = tp <= 4 ? elems < 3 * (int64_t{1} << 19) : elems <= (int64_t{1} << 21);
-      deep_ring = !direct;
-    } else {
-      direct = T_pad * H <= (int64_t{1} << (H <= 1024 ? 22 : 20));
-    }
+    direct = (rows_x_h <= (int64_t{1} << 20) && (tp < 12 || H < 3072 || elems <= 12600000)) ||
+             (!nvfp4 && tp <= 4 && rows_x_h <= 1400000) ||
+             (!nvfp4 && tp <= 8 && rows_x_h <= 1200000) ||
+             (H <= 1024 && rows_x_h <= (int64_t{1} << 22));
+    if (direct && !nvfp4 && tp <= 4 && rows_x_h >= (int64_t{1} << 18) && rows_x_h <= 800000)
+      vec = 2;
+    if (!direct && H >= 3072 && T_pad <= 4 * kSmsHint)
+      one_round = static_cast<int>((T_pad + kSmsHint - 1) / kSmsHint);
   } else if (H <= 8192) {
-    if (tp >= 12)
-      split = T_pad <= 16 ? 8 : (T_pad <= 64 ? 4 : 0);
-    else if (tp >= 6)
-      split = T_pad <= 8 ? 8 : (T_pad <= 32 ? 4 : (T_pad <= 64 ? 2 : 0));
-    else if (tp >= 2 && H >= 7168)
-      split = T_pad <= 8 ? 8 : 0;
-    direct = split > 0 || elems <= (int64_t{1} << 20) || (tp >= 12 && T_pad <= 128);
-    deep_ring_1 = !direct && T_pad >= 64 && T_pad <= 128;
+    if (tp <= 5) {
+      split = (tp >= 2 && H >= 6144 && T_pad <= 16) ? 8 : 0;
+    } else if (tp < 12) {
+      split = T_pad <= 12 ? 8 : (T_pad <= 64 ? ((H >= 6144 || T_pad <= 32) ? 4 : 2) : 0);
+    } else {
+      split = T_pad <= 16 ? (H >= 7168 ? 8 : 4) : (T_pad <= 64 ? 4 : 0);
+    }
+    if (split) {
+      direct = true;
+    } else if (tp < 12) {
+      if (T_pad <= 128 || (tp <= 3 && H >= 7168 && T_pad <= 160)) {
+        direct = true;
+      } else if (H <= 5120 && T_pad <= 224) {
+        direct = true;
+        split = 2;
+      } else if (H <= 6144 && T_pad <= 160) {
+        direct = true;
+        split = 4;
+      }
+    } else if (T_pad <= 96 || (T_pad <= 128 && H < 8192)) {
+      direct = true;
+    } else if (T_pad <= 128) {
+      ring_1 = true;
+    }
+    if (!direct && !ring_1 && H <= 6144 && T_pad > kSmsHint && T_pad <= 4 * kSmsHint)
+      one_round = static_cast<int>((T_pad + kSmsHint - 1) / kSmsHint);
   } else {
-    if (tp >= 12)
-      split = T_pad <= 64 ? 8 : 0;
-    else if (tp >= 6)
-      split = T_pad <= 32 ? 8 : (T_pad <= 64 ? 4 : 0);
-    else if (tp >= 2)
-      split = T_pad <= 16 ? 8 : (tp >= 3 && T_pad <= 32 ? 4 : 0);
-    direct = split > 0 || T_pad <= 32;
+    split = tp < 2                      ? 0
+          : T_pad <= (tp <= 5 ? 16 : 24) ? 8
+          : T_pad <= 64                   ? 4
+          : (T_pad <= 80 && H <= 12288)   ? 8
+                                          : 0;
+    direct = split > 0 || (tp <= 5 && (T_pad <= 96 || (T_pad <= 128 && H <= 12288)));
   }
   if (direct) {
     c.kernel = SP_KERNEL_DIRECT;
-    c.vec_per_thread = (split > 0 || H <= 4096) ? 1 : (H <= 8192 ? 2 : 4);
+    c.vec_per_thread = split > 0 ? 1 : (vec ? vec : (H <= 4096 ? 1 : (H <= 8192 ? 2 : 4)));
     c.ctas_per_sm = H <= 4096 ? 16 : 8;
     c.stages = 0;
     c.split = split;
-  } else if (deep_ring && c.kernel == SP_KERNEL_STAGED && max_stages(H, 2) >= c.stages) {
-    c.ctas_per_sm = 2;
-    c.stages = 0;  // as many as fit
-  } else if (deep_ring_1 && c.kernel == SP_KERNEL_STAGED && max_stages(H, 1) >= c.stages) {
+  } else if (ring_1 && c.kernel == SP_KERNEL_STAGED && max_stages(H, 1) >= c.stages) {
     c.ctas_per_sm = 1;
+    c.stages = 0;  // as many as fit
+  } else if (one_round > 0 && c.kernel == SP_KERNEL_STAGED &&
+             max_stages(H, one_round) >= c.stages) {
+    // All rows fit in one round of this grid: each CTA has at most one row, so use only as many
+    // CTAs per SM as the rows need and give each the deepest ring that fits.
+    c.ctas_per_sm = one_round;
     c.stages = 0;
-  } else if (!direct && c.kernel == SP_KERNEL_STAGED && H > 4096 && H <= 6144 &&
-             T_pad > kSmsHint && T_pad <= kSmsHint * c.ctas_per_sm) {
-    // All rows fit in one round of the large-call grid: each CTA has at most one row, so use
-    // only as many CTAs per SM as the rows need and give each the deepest ring that fits.
-    const int want = static_cast<int>((T_pad + kSmsHint - 1) / kSmsHint);
-    if (max_stages(H, want) >= c.stages) {
-      c.ctas_per_sm = want;
-      c.stages = 0;
-    }
   } else if (!direct && c.kernel == SP_KERNEL_STAGED && H >= 4096 &&
              T_pad > kSmsHint * c.ctas_per_sm && T_pad < 2 * kSmsHint * c.ctas_per_sm) {
     // Between one and two rounds of rows: the second round runs part-empty. Take the CTAs per

@@ -99,54 +99,75 @@ def test_launch_selection(lib):
 
 
 @pytest.mark.parametrize("tp,T,H,want", [
-    (2, 64, 1024, (1, 1, 16, 0)),       # tiny: direct, one vector per thread
-    (4, 64, 4096, (1, 1, 16, 0)),       # 1M partial elements, tp <= 4: direct
-    (4, 128, 4096, (0, 2, 2, 0)),       # 2M, few rows: staged, deep ring at 2 CTAs/SM
-    (8, 64, 4096, (1, 1, 16, 0)),       # 2M, tp > 4: direct
-    (16, 64, 4096, (1, 1, 16, 0)),      # tp >= 6: direct while T * H <= 2^20
+    # H <= 4096: direct while T * H <= 2^20 (2^22 for H <= 1024), one vector per thread ...
+    (2, 64, 1024, (1, 1, 16, 0)),
+    (8, 64, 4096, (1, 1, 16, 0)),
+    (16, 64, 4096, (1, 1, 16, 0)),
     (16, 256, 2048, (1, 1, 16, 0)),
-    (5, 160, 4096, (0, 2, 2, 0)),       # tp = 5: deep ring above 2M partial elements
-    (8, 512, 2048, (1, 1, 16, 0)),      # T > 256: direct while T * H <= 2^20
-    (4, 4096, 1024, (1, 1, 16, 0)),     # ... 2^22 for H <= 1024
+    (8, 512, 2048, (1, 1, 16, 0)),
+    (4, 4096, 1024, (1, 1, 16, 0)),
     (4, 8192, 1024, (0, 2, 16, 4)),
-    (4, 32, 8192, (1, 2, 8, 0)),        # 4096 < H <= 8192: direct while tp*T*H <= 2^20
-    (4, 64, 8192, (0, 2, 1, 0)),        # 2M: the staged kernel
-    # split rows: a cluster of 8 or 4 CTAs per row, one vector per thread
-    (8, 8, 8192, (1, 1, 8, 0, 8)),
-    (8, 32, 5120, (1, 1, 8, 0, 4)),
-    (8, 40, 5120, (1, 1, 8, 0, 2)),     # 33-64 rows at 6 <= tp < 12: 2 CTAs per row
-    (8, 72, 5120, (0, 2, 1, 0)),        # more rows: no split
-    (16, 16, 7168, (1, 1, 8, 0, 8)),
-    (16, 64, 8192, (1, 1, 8, 0, 4)),
-    (16, 80, 8192, (1, 2, 8, 0)),       # tp >= 12: direct up to 128 rows
-    (16, 144, 8192, (0, 2, 2, 4)),
-    (2, 8, 7168, (1, 1, 8, 0, 8)),
-    (4, 8, 5120, (1, 2, 8, 0)),         # tp < 6 splits only from H = 7168
-    (4, 16, 8192, (1, 2, 8, 0)),
-    (8, 8, 4096, (1, 1, 16, 0)),        # never at H <= 4096
-    (1, 8, 8192, (1, 2, 8, 0)),
-    # H > 8192: split rows, else direct with four vectors per thread, for few rows
-    (2, 16, 16384, (1, 1, 8, 0, 8)),
-    (2, 32, 16384, (1, 4, 8, 0)),
-    (4, 32, 12288, (1, 1, 8, 0, 4)),
-    (2, 32, 12288, (1, 4, 8, 0)),
-    (4, 64, 12288, (0, 4, 1, 4)),
-    (8, 32, 12288, (1, 1, 8, 0, 8)),
-    (8, 64, 16384, (1, 1, 8, 0, 4)),
-    (8, 72, 16384, (0, 4, 1, 4)),
-    (16, 64, 16384, (1, 1, 8, 0, 8)),
-    (16, 128, 16384, (0, 4, 1, 4)),
-    (8, 72, 8192, (0, 2, 1, 0)),        # 64-128 rows: one CTA per SM, deepest ring
-    (4, 128, 7168, (0, 2, 1, 0)),
-    (16, 256, 7168, (0, 2, 2, 4)),
-    (8, 256, 5120, (0, 2, 2, 0)),       # one round of rows at H = 5120: 2 CTAs/SM, deep ring
-    (8, 384, 5120, (0, 2, 3, 0)),
-    (8, 512, 5120, (0, 2, 2, 0)),       # 1.1 rounds at 3 CTAs/SM: 2 CTAs/SM fill the last one
+    (8, 8, 4096, (1, 1, 16, 0)),        # never split at H <= 4096
+    # ... two at tp <= 4 for 2^18 <= T * H <= 800 K, and up to 1.4 M (tp <= 4) / 1.2 M (tp <= 8)
+    (4, 64, 4096, (1, 2, 16, 0)),
+    (4, 128, 4096, (1, 2, 16, 0)),
+    (5, 160, 4096, (1, 1, 16, 0)),
+    (4, 320, 4096, (1, 1, 16, 0)),
+    (8, 384, 3072, (1, 1, 16, 0)),
+    # then one round of rows (H >= 3072): ceil(T / 152) CTAs per SM, deepest ring
+    (16, 320, 3072, (0, 2, 3, 0)),
     (4, 768, 4096, (0, 2, 3, 0)),       # 1.3 rounds at 4 CTAs/SM: 3 fill it better
     (4, 1024, 4096, (0, 2, 4, 3)),      # fewer CTAs would leave each more than 3 rows
+    # 4096 < H <= 8192: split rows, a cluster of 8, 4 or 2 CTAs per row, one vector per thread
+    (8, 8, 8192, (1, 1, 8, 0, 8)),
+    (6, 12, 8192, (1, 1, 8, 0, 8)),
+    (8, 32, 5120, (1, 1, 8, 0, 4)),
+    (8, 40, 5120, (1, 1, 8, 0, 2)),     # 33-64 rows at H = 5120, 6 <= tp < 12: 2 per row
+    (6, 48, 5120, (1, 1, 8, 0, 2)),
+    (16, 16, 7168, (1, 1, 8, 0, 8)),
+    (16, 64, 8192, (1, 1, 8, 0, 4)),
+    (2, 8, 7168, (1, 1, 8, 0, 8)),
+    (4, 8, 5120, (1, 2, 8, 0)),         # tp <= 5 splits from H = 6144
+    (4, 16, 8192, (1, 1, 8, 0, 8)),
+    (1, 8, 8192, (1, 2, 8, 0)),         # a single partial: no split
+    # then direct, two vectors per thread, up to 128 rows (tp >= 12: 96, or 128 below 7168)
+    (4, 32, 8192, (1, 2, 8, 0)),
+    (4, 64, 8192, (1, 2, 8, 0)),
+    (8, 72, 5120, (1, 2, 8, 0)),
+    (8, 72, 8192, (1, 2, 8, 0)),
+    (4, 128, 7168, (1, 2, 8, 0)),
+    (2, 160, 8192, (1, 2, 8, 0)),       # tp <= 3 at H >= 7168: up to 160 rows
+    (16, 80, 8192, (1, 2, 8, 0)),
+    (16, 112, 5120, (1, 2, 8, 0)),
+    (16, 112, 8192, (0, 2, 1, 0)),      # tp >= 12, 97-128 rows at H = 8192: deep ring, 1/SM
+    (16, 112, 7168, (1, 2, 8, 0)),
+    (8, 192, 5120, (1, 1, 8, 0, 2)),    # split 2 up to 224 rows at H = 5120
+    (6, 160, 6144, (1, 1, 8, 0, 4)),    # split 4 up to 160 rows at H = 6144
+    (8, 256, 5120, (0, 2, 2, 0)),       # one round of rows at H <= 6144, deepest ring
+    (8, 384, 5120, (0, 2, 3, 0)),
+    (6, 384, 6144, (0, 2, 3, 0)),
+    (8, 512, 5120, (0, 2, 2, 0)),       # 1.1 rounds at 3 CTAs/SM: 2 CTAs/SM fill the last one
+    (16, 144, 8192, (0, 2, 2, 4)),
+    (16, 256, 7168, (0, 2, 2, 4)),
     (8, 384, 7168, (0, 2, 1, 0)),       # 1.3 rounds at 2 CTAs/SM; long rows: one CTA per SM
     (4, 384, 7168, (0, 2, 2, 4)),       # ... but not at tp = 4
-    (4, 4096, 4096, (0, 2, 4, 3)),      # large: staged, CTAs/SM = 16384 / H
+    # H > 8192: split rows, else (tp <= 5) direct with four vectors per thread, for few rows
+    (2, 16, 16384, (1, 1, 8, 0, 8)),
+    (2, 32, 16384, (1, 1, 8, 0, 4)),
+    (8, 24, 16384, (1, 1, 8, 0, 8)),
+    (4, 32, 12288, (1, 1, 8, 0, 4)),
+    (4, 64, 12288, (1, 1, 8, 0, 4)),
+    (8, 32, 12288, (1, 1, 8, 0, 4)),
+    (8, 64, 16384, (1, 1, 8, 0, 4)),
+    (16, 64, 16384, (1, 1, 8, 0, 4)),
+    (8, 80, 12288, (1, 1, 8, 0, 8)),
+    (4, 96, 16384, (1, 4, 8, 0)),
+    (4, 128, 12288, (1, 4, 8, 0)),
+    (4, 128, 16384, (0, 4, 1, 4)),
+    (8, 72, 16384, (0, 4, 1, 4)),
+    (16, 128, 16384, (0, 4, 1, 4)),
+    # large calls: staged, CTAs/SM = 16384 / H
+    (4, 4096, 4096, (0, 2, 4, 3)),
     (8, 8192, 7168, (0, 2, 2, 4)),
     (8, 16384, 5120, (0, 2, 3, 4)),
 ])

@@ -627,15 +627,22 @@ def test_dynamic_schedule_soak_two_chained_streams():
 # ------------------------------------------------------------------------- launch-rule bands
 @pytest.mark.parametrize("tp,T,H,mode,band", [
     (4, 32, 8192, "fp8_per_token", (1, 2, 8, 0)),     # direct, two vectors per thread
-    (4, 128, 4096, "none", (0, 2, 2, 0)),             # staged, deep ring at 2 CTAs/SM
+    (4, 128, 4096, "none", (1, 2, 16, 0)),            # direct, two vectors at tp <= 4
+    (8, 384, 3072, "fp8_per_token", (1, 1, 16, 0)),   # direct up to 1.2 M at tp <= 8
     (16, 128, 2048, "fp8_static", (1, 1, 16, 0)),     # direct at tp >= 6
     (16, 16, 8192, "fp8_per_token", (1, 1, 8, 0, 8)), # split rows, 8 CTAs per row
     (8, 32, 5120, "nvfp4", (1, 1, 8, 0, 4)),          # split rows, 4 CTAs per row
-    (8, 48, 7168, "fp8_per_token", (1, 1, 8, 0, 2)),  # split rows, 2 CTAs per row
-    (16, 96, 5120, "nvfp4", (1, 2, 8, 0)),            # direct up to 128 rows at tp >= 12
-    (2, 24, 16384, "fp8_static", (1, 4, 8, 0)),       # direct, four vectors per thread
-    (16, 48, 12288, "nvfp4", (1, 1, 8, 0, 8)),        # split rows at H > 8192
-    (8, 96, 7168, "nvfp4", (0, 2, 1, 0)),             # staged, one CTA per SM
+    (8, 48, 5120, "fp8_per_token", (1, 1, 8, 0, 2)),  # split rows, 2 CTAs per row
+    (8, 192, 5120, "nvfp4", (1, 1, 8, 0, 2)),         # split 2 up to 224 rows at H = 5120
+    (6, 156, 6144, "fp8_static", (1, 1, 8, 0, 4)),    # split 4 up to 160 rows at H = 6144
+    (16, 96, 5120, "nvfp4", (1, 2, 8, 0)),            # direct up to 128 rows below H = 7168
+    (2, 24, 16384, "fp8_static", (1, 1, 8, 0, 4)),    # split rows at H > 8192, tp <= 5
+    (4, 96, 16384, "nvfp4", (1, 4, 8, 0)),            # direct, four vectors per thread
+    (16, 48, 12288, "nvfp4", (1, 1, 8, 0, 4)),        # split rows at H > 8192
+    (8, 80, 12288, "fp8_per_token", (1, 1, 8, 0, 8)), # 8 CTAs per row up to 80 rows
+    (16, 112, 8192, "nvfp4", (0, 2, 1, 0)),           # staged, one CTA per SM
+    (16, 320, 3072, "none", (0, 2, 3, 0)),            # one round of rows at H = 3072
+    (6, 384, 6144, "fp8_per_token", (0, 2, 3, 0)),    # one round of rows at H = 6144
     (8, 256, 5120, "fp8_static", (0, 2, 2, 0)),       # one round of rows, fewest CTAs
     (4, 768, 4096, "none", (0, 2, 3, 0)),             # last round filled at 3 CTAs/SM
     (8, 512, 5120, "fp8_per_token", (0, 2, 2, 0)),    # last round filled at 2 CTAs/SM
