@@ -618,12 +618,19 @@ def run_kernel_only(args) -> None:
         print(json.dumps({"workload": FC2_WORKLOAD, **r}), flush=True)
         return
     w = synth.workload(args.workload if not str(args.workload).isdigit() else int(args.workload))
+    if args.shape:  # tp,T,H[,mode]: the workload's distributions at another shape (all rows valid)
+        parts = args.shape.split(",")
+        tp, T, H = (int(x) for x in parts[:3])
+        w.update(tp=tp, T_pad=T, T_valid=T, H=H, name=f"{w['name']}@tp{tp}_T{T}_H{H}")
+        if len(parts) > 3:
+            w["mode"] = parts[3]
     if args.rows:  # a multiple of tp, with as many padding rows as the full workload
         pad = w["T_pad"] - w["T_valid"]
         w["T_pad"] = max(w["tp"], min(w["T_pad"], args.rows) // w["tp"] * w["tp"])
         w["T_valid"] = max(0, w["T_pad"] - pad)
+    base_name = w["name"].split("@")[0]
     base = Problem(w, synth.BASE_SEED + 1 + synth.WORKLOADS.index(
-        next(x for x in synth.WORKLOADS if x["name"] == w["name"])), device, sp)
+        next(x for x in synth.WORKLOADS if x["name"] == base_name)), device, sp)
     sets = max(2, min(8, -(-(4 * L2_BYTES) // base.nbytes())))
     problems = [base] + [Problem(w, base.inp["seed"] + 1000 * k, device, sp)
                          for k in range(1, sets)]
@@ -738,6 +745,8 @@ def main() -> None:
                     help="only warm-up + timed kernel launches of the workload (for profilers)")
     ap.add_argument("--rows", type=int, default=0,
                     help="with --kernel-only: use only the first ROWS padded rows")
+    ap.add_argument("--shape", default="",
+                    help="with --kernel-only: tp,T,H[,mode] at the workload's distributions")
     ap.add_argument("--reference-budget-s", type=float, default=60.0,
                     help="CPU seconds for the whole reference-arm run (bounded row samples)")
     args = ap.parse_args()

@@ -338,7 +338,9 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
   const int vend = kSplit > 1 ? min(vbase + p.split_chunk, p.nvec) : p.nvec;
   const int vc = vbase + c;  // this thread's first vector
   bool setup_seen = false;  // split rows: waited on the set-up cluster barrier
-  if constexpr (kSplit > 1) cluster_arrive();  // the set-up barrier (cluster_row_sum)
+  // the set-up barrier (cluster_row_sum): it orders no data, so the arrival is relaxed (one
+  // `membar` fewer on the row's path: 1-6 % faster on decode calls, GB300 A/B)
+  if constexpr (kSplit > 1) cluster_arrive_relaxed();
   pdl_launch_dependents();
   pdl_wait_prerequisites();
   uint4 w[kVec], b[kVec];
