@@ -28,8 +28,11 @@
  *
  * Conventions for every entry point:
  *   - All tensor arguments are DEVICE pointers into the memory of the current CUDA device, unless
- *     the argument says "host". The caller owns every buffer; the library allocates nothing, keeps
- *     no per-call state and may be called concurrently from several host threads.
+ *     the argument says "host". The caller owns every buffer; the library allocates nothing and
+ *     may be called concurrently from several host threads. What it keeps between calls is
+ *     listed where it is used: the device error word (sp_device_error), the dynamic row
+ *     schedule's per-stream counters (sp_fused_options.row_counter), the no-allocation entry's
+ *     counter (sp_fused_reduce_norm_noalloc) and each host thread's last launch (sp_last_launch).
  *   - bf16 is IEEE binary32's top 16 bits; FP8 E4M3 is the OCP "E4M3" (fn) format; E2M1 is the
  *     OCP MX FP4 format. All tensors are dense, row-major, C-contiguous.
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream); nothing synchronises the
