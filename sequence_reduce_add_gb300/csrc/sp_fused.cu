@@ -54,10 +54,7 @@ bool overlaps(const void* p, int64_t pn, const void* q, int64_t qn) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// The checks of sp_fused_reduce_norm, in the documented order. The shape rules restate the
-// shard checks of the PR #18671 notes (§5.2): the padded token count is a whole number of
-// equal shards, and the valid tokens fit in it.
-// What sp_fused_reduce_norm_ex adds to the plain call (defaults: 1 and none).
+// What sp_fused_reduce_norm_ex adds to the plain call (the defaults give the plain call).
 struct Extras {
   float partial_scale = 1.0f;
   const void* addend = nullptr;
@@ -69,6 +66,9 @@ struct Extras {
   int64_t withhold = -1;            // self-test: CTA 0 withholds this ring fill (else -1)
 };
 
+// The checks of sp_fused_reduce_norm, in the documented order. The shape rules restate the
+// shard checks of the PR #18671 notes (§5.2): the padded token count is a whole number of
+// equal shards, and the valid tokens fit in it.
 sp_status check(const void* partials, int tp, int64_t T_pad, int64_t T_valid, int64_t H,
                 const void* residual, const void* weight, const void* bias, float eps, int mode,
                 const float* scale, const void* out, const void* out_scales,
@@ -243,9 +243,6 @@ int max_stages(int64_t H, int ctas_per_sm) {
   return s > 64 ? 64 : s;
 }
 
-// Grid of a persistent launch: SMs x CTAs per SM, where CTAs per SM is the requested number
-// capped at what the SM can hold for this kernel (registers, threads, shared memory), so the
-// grid is never a ragged second wave; and never more CTAs than rows.
 // Resident CTAs per SM of (kernel, threads, smem) on the current device, cached: the occupancy
 // query costs about a microsecond, as much as the launch of a small problem.
 struct OccupancyKey {
@@ -298,6 +295,9 @@ cudaError_t resident_ctas(Kernel kernel, int threads, int smem, int device, int*
   return cudaSuccess;
 }
 
+// Grid of a persistent launch: SMs x CTAs per SM, where CTAs per SM is the requested number
+// capped at what the SM can hold for this kernel (registers, threads, shared memory), so the
+// grid is never a ragged second wave; and never more CTAs than rows.
 template <typename Kernel>
 cudaError_t persistent_grid(Kernel kernel, int threads, int smem, int ctas_per_sm,
                             int64_t rows, const DeviceInfo* dev, int* grid) {
@@ -313,7 +313,8 @@ cudaError_t persistent_grid(Kernel kernel, int threads, int smem, int ctas_per_s
 }
 
 // Launch with programmatic stream serialisation: the kernel may be scheduled while the previous
-// kernel of the stream finishes; it waits (griddepcontrol.wait) before touching global memory.
+// kernel of the stream finishes; it waits (griddepcontrol.wait) before it reads or writes global
+// memory (an L2 prefetch, which changes no memory, may come before).
 template <typename Kernel, typename KParams>
 cudaError_t launch_pdl(Kernel kernel, int grid, int threads, int smem, cudaStream_t stream,
                        const KParams& p) {
