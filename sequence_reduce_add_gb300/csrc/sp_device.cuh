@@ -338,50 +338,75 @@ __device__ __forceinline__ int cluster_rank() {
   asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
   return static_cast<int>(r);
 }
-// The cluster barrier in two halves: every thread of every CTA arrives (its earlier writes,
-// shared-memory writes to other CTAs included, are released), and a thread's wait returns once
-// all threads of the cluster have arrived. A thread waits before it arrives again.
-__device__ __forceinline__ void cluster_arrive() {
-  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
-}
-// The same arrival without release semantics, for a barrier that orders no data (a barrier whose
-// wait only has to show that every thread of the cluster is running).
+// The set-up cluster barrier in two halves: every thread of every CTA arrives at the start, and
+// a thread's wait returns once all threads of the cluster have arrived (every CTA is running, and
+// what each initialised before its arrival can be used by the others).
+// The arrival has no release semantics: the barrier orders no data of its own (the exchange
+// barriers' initialisation is released by fence.mbarrier_init before it).
 __device__ __forceinline__ void cluster_arrive_relaxed() {
   asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
 __device__ __forceinline__ void cluster_wait() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
-// Two floats into CTA `rank`'s copy of this CTA's shared-memory address `addr`.
-__device__ __forceinline__ void st_cluster_f32x2(uint32_t addr, int rank, float2 v) {
-  uint32_t remote;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(remote) : "r"(addr), "r"(rank));
-  asm volatile("st.shared::cluster.v2.f32 [%0], {%1, %2};" ::"r"(remote), "f"(v.x), "f"(v.y)
-               : "memory");
+// Two floats into CTA `rank`'s copy of this CTA's shared-memory address `addr`, completing 8 bytes
+// of transaction on that CTA's copy of the mbarrier at `bar`: an asynchronous store whose arrival
+// the receiver sees through its barrier, with no fence on the sender's side.
+__device__ __forceinline__ void st_async_f32x2(uint32_t addr, uint32_t bar, int rank, float2 v) {
+  uint32_t raddr, rbar;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(raddr) : "r"(addr), "r"(rank));
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(rbar) : "r"(bar), "r"(rank));
+  asm volatile(
+      "st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.f32 [%0], {%1, %2}, [%3];" ::"r"(
+          raddr),
+      "f"(v.x), "f"(v.y), "r"(rbar)
+      : "memory");
 }
 // Split rows: the exchange of each row's (sum of squares, max) between the CTAs of a cluster.
-// Threads 0 .. kSplit-1 push the CTA-wide pair into slot [row parity][own rank] of every CTA of
-// the cluster (one peer each), a cluster barrier makes the pushes visible, and each CTA adds the
-// kSplit pairs from its own shared memory in rank order, so every CTA gets the same bits. Slots
-// alternate between rows: a CTA pushes into slot p again two rows later, after the barrier of
-// the row in between, which every CTA reaches only after reading slot p. The first exchange
-// first waits on the set-up barrier every CTA arrived at when it started (no CTA writes into a
-// peer that is not yet running); nothing is accessed in a peer after the last row's barrier, so
-// a CTA may exit right after it. The barriers are the hardware cluster barrier: every CTA of the
-// cluster walks the same rows, so all take the same barriers, and no wait here can time out.
-__shared__ float2 g_xslots[2][8];  // this CTA's [row parity][source rank] pairs
+// Every CTA holds two slot sets and two mbarriers (count 1), one of each per row parity. For a
+// row of parity q, thread 0 arrives on barrier q expecting kSplit * 8 bytes, threads 0 .. kSplit-1
+// push the CTA-wide pair into slot [q][own rank] of CTA 0 .. kSplit-1 (one peer each, this CTA
+// included) with st.async, which completes 8 bytes on that CTA's barrier q, and every thread
+// waits for the barrier's phase; then each CTA adds the kSplit pairs in rank order, so every CTA
+// gets the same bits. The n-th exchanged row of a CTA uses parity n & 1 and waits on phase
+// (n >> 1) & 1 of that barrier.
+// Reuse: a CTA pushes into slot set q (and completes barrier q) for row n + 2 only after its own
+// wait for row n + 1, which needs every CTA's push for row n + 1; a CTA pushes for row n + 1
+// only after all of its threads have read the slots of row n (the row's block barrier lies in
+// between) and after barrier q's phase for row n has completed. A push that arrives before the
+// receiver's own arrival only makes the transaction count negative for a while.
+// Start: each CTA initialises its barriers and fences the initialisation before its arrival at
+// the set-up cluster barrier; the first exchange waits on that barrier first, so no CTA pushes
+// into a peer that is not running or whose barriers are not ready. End: a CTA's last wait
+// returns only once every push into it has landed, so it may exit right after.
+// The wait is bounded (kWaitLimitNs): if it runs out (a peer stalled for seconds), the error bit
+// goes to the launch's error word and the thread waits once more, with the same bound, so that a
+// late push still lands in a running CTA.
+__shared__ float2 g_xslots[2][8];            // this CTA's [row parity][source rank] pairs
+__shared__ __align__(8) uint64_t g_xbar[2];  // this CTA's [row parity] exchange barriers
+
+__device__ __forceinline__ void cluster_exchange_init() {
+  mbar_init(smem_addr(&g_xbar[0]), 1);
+  mbar_init(smem_addr(&g_xbar[1]), 1);
+  fence_mbar_init();
+}
 
 template <int kSplit>
 __device__ __forceinline__ float2 cluster_row_sum(float2 part, int rank, int parity,
-                                                  bool& setup_seen) {
+                                                  uint32_t phase, bool& setup_seen,
+                                                  unsigned int* error_word) {
   if (!setup_seen) {
     cluster_wait();
     setup_seen = true;
   }
+  const uint32_t bar = smem_addr(&g_xbar[parity]);
+  if (threadIdx.x == 0) mbar_arrive_expect_tx(bar, kSplit * 8u);
   if (threadIdx.x < kSplit)
-    st_cluster_f32x2(smem_addr(&g_xslots[parity][rank]), static_cast<int>(threadIdx.x), part);
-  cluster_arrive();
-  cluster_wait();
+    st_async_f32x2(smem_addr(&g_xslots[parity][rank]), bar, static_cast<int>(threadIdx.x), part);
+  if (!mbar_wait_bounded(bar, phase, nullptr)) {
+    if (threadIdx.x == 0) atomicOr(error_word, kErrWaitTimeout);
+    mbar_wait_bounded(bar, phase, nullptr);
+  }
   float ss = 0.0f, mx = 0.0f;
 #pragma unroll
   for (int r = 0; r < kSplit; ++r) {
@@ -513,13 +538,13 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
                                           const uint4 (&w)[kVec], const QuantConst& qc,
                                           RedSlot* slots, int parity, int c, int abort,
                                           int vbase = 0, int vend = 0, int rank = 0,
-                                          bool* setup_seen = nullptr) {
+                                          bool* setup_seen = nullptr, uint32_t xphase = 0) {
   const int64_t H = p.H;
   const int v0 = kSplit > 1 ? vbase : 0;
   const int vlim = kSplit > 1 ? vend : p.nvec;
   float ss0 = 0.0f, ss1 = 0.0f;  // sums of squares of the even and the odd elements
-  // Split rows: the new residual is stored after the exchange, whose release would otherwise
-  // wait for these stores to complete.
+  // Split rows: the new residual is stored after the exchange (storing it before measured the
+  // same to 1.5 % slower on decode calls, GB300 A/B).
   uint4 res[kSplit > 1 ? kVec : 1];
 #pragma unroll
   for (int k = 0; k < kVec; ++k) {
@@ -548,7 +573,7 @@ __device__ __forceinline__ int finish_row(const Params& p, int64_t t, float (&h)
   float2 red =
       row_reduce<kMode == kModeFp8PerToken>(ss, mx, abort, slots, parity, p.nthreads, &abort_all);
   if constexpr (kSplit > 1) {
-    red = cluster_row_sum<kSplit>(red, rank, parity, *setup_seen);
+    red = cluster_row_sum<kSplit>(red, rank, parity, xphase, *setup_seen, p.error_word);
 #pragma unroll
     for (int k = 0; k < kVec; ++k) {
       const int v = v0 + c + k * p.nthreads;

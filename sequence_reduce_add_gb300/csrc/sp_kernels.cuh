@@ -338,17 +338,21 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
   const int vend = kSplit > 1 ? min(vbase + p.split_chunk, p.nvec) : p.nvec;
   const int vc = vbase + c;  // this thread's first vector
   bool setup_seen = false;  // split rows: waited on the set-up cluster barrier
-  // the set-up barrier (cluster_row_sum): it orders no data, so the arrival is relaxed (one
-  // `membar` fewer on the row's path: 1-6 % faster on decode calls, GB300 A/B)
-  if constexpr (kSplit > 1) cluster_arrive_relaxed();
+  // split rows: the exchange barriers, then the set-up cluster barrier (cluster_row_sum)
+  if constexpr (kSplit > 1) {
+    if (c == 0) cluster_exchange_init();
+    cluster_arrive_relaxed();
+  }
   pdl_launch_dependents();
   pdl_wait_prerequisites();
   uint4 w[kVec], b[kVec];
   load_row_constants<kVec, kSplit>(p, c, w, b, vbase, vend);
   const QuantConst qc = load_quant_const<kMode>(p);
 
-  int parity = 0;
-  // every CTA of a cluster takes the same rows, so all meet the same cluster barriers
+  // rows finished so far (padding rows aside): the row's parity is its low bit, and for split
+  // rows the phase of the exchange barrier it waits on is the next bit
+  unsigned done = 0;
+  // every CTA of a cluster takes the same rows, so all take part in the same exchanges
   for (int64_t t = blockIdx.x / kSplit; t < p.rows_total; t += gridDim.x / kSplit) {
     if (t >= p.T_valid) {
       zero_row<kVec, kMode, kSplit>(p, t, c, vbase, vend);
@@ -437,9 +441,9 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
     }
 #pragma unroll
     for (int k = 0; k < kVec; ++k) add_bf16x8(b[k], h[k]);
-    finish_row<kVec, kMode, kSplit>(p, t, h, w, qc, slots, parity, c, 0, vbase, vend, rank,
-                                    &setup_seen);
-    parity ^= 1;
+    finish_row<kVec, kMode, kSplit>(p, t, h, w, qc, slots, static_cast<int>(done & 1u), c, 0,
+                                    vbase, vend, rank, &setup_seen, (done >> 1) & 1u);
+    ++done;
   }
   // A CTA that made no exchange still completes the set-up barrier it arrived at.
   if constexpr (kSplit > 1) {
