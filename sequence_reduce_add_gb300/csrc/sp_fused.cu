@@ -640,22 +640,31 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   //                     12.6 M), or, except for NVFP4 output, T * H <= 1.4 M at tp <= 4 (1.2 M at
   //                     tp <= 8); two vectors per thread at tp <= 4 and 2^18 <= T * H <= 800 K
   //                     (not for NVFP4; up to 27 % faster than the deep ring this replaced at
-  //                     tp <= 5); else, for H >= 3072 and at most four rounds of 152 rows,
-  //                     ceil(T / 152) CTAs per SM with every stage that fits (15-40 % faster at
-  //                     T = 320-448);
-  //   4096 < H <= 8192: split rows: 2 <= tp <= 5 and H >= 6144, 8 CTAs per row up to 16 rows;
-  //                     6 <= tp < 12, 8 up to 12 rows and 4 up to 64 (at H = 5120, 4 up to 32
-  //                     and 2 up to 64); tp >= 12, 8 up to 16 rows (4 below H = 7168) and 4 up
-  //                     to 64. Then direct with two vectors per thread up to 128 rows (160 at
+  //                     tp <= 5); above H = 3072 (tp >= 2) split rows, 4 CTAs per row up to 16
+  //                     rows and, except for NVFP4, up to 24 (32 at tp <= 5), then 8 per row up
+  //                     to 48 rows at tp <= 5; else, for H >= 3072 and at most four rounds of 152
+  //                     rows, ceil(T / 152) CTAs per SM with every stage that fits (15-40 %
+  //                     faster at T = 320-448);
+  //   4096 < H <= 8192: split rows: 2 <= tp <= 5, 8 CTAs per row up to 16 rows (NVFP4 below
+  //                     H = 6144: 4); 6 <= tp < 12, 8 up to 12 rows and 4 up to 64 (at
+  //                     H = 5120, 4 up to 32 and 2 up to 64), and at H <= 5120 4 for 65-96 rows
+  //                     (NVFP4 from H = 4609); tp >= 12, 8 up to 16 rows (4 below H = 7168) and
+  //                     4 up to 64 (2 for 33-64 rows at H <= 5120, not for NVFP4), 4 for 65-80
+  //                     rows at H >= 7168 and for 65-96 at H <= 5120 (NVFP4 from H = 4609, and
+  //                     up to 128 rows). Then direct with two vectors per thread up to 128 rows (160 at
   //                     tp <= 3 and H >= 7168; at tp >= 12 up to 96, or 128 below H = 8192:
   //                     15-36 % faster than the one-CTA-per-SM deep ring it replaced), split 2 up
   //                     to 224 rows at H = 5120 and split 4 up to 160 at H = 6144 (tp < 12); the
   //                     deep ring at one CTA per SM for tp >= 12 and 97-128 rows at H = 8192; one
   //                     round of rows for H <= 6144 (17-41 % faster at H = 6144, T = 320-384);
   //   H > 8192:         split rows (tp >= 2): 8 CTAs per row up to 16 rows (24 at tp >= 6), 4 up
-  //                     to 64, 8 up to 80 at H <= 12288 (16-36 % faster); then at tp <= 5 direct
-  //                     with four vectors per thread up to 96 rows (128 at H <= 12288); else
-  //                     staged.
+  //                     to 64 (8 above H = 12288 at tp <= 5), 8 up to 80 at H <= 12288 (16-36 %
+  //                     faster); then at tp <= 5 direct with four vectors per thread up to 96
+  //                     rows (128 at H <= 12288); else staged.
+  // The split bands were widened once the split kernel combined a row's sums with asynchronous
+  // pushes instead of a cluster barrier per row: over 796 shapes swept again (tp 2-16, H 2048-
+  // 16384, T 8-128, bf16, per-token FP8 and NVFP4 output) the new bands are 2.1 % faster summed
+  // (up to 24 % on one shape: tp 16, H 5120, 96 rows) and slower on none by more than 1 %.
   const int64_t elems = static_cast<int64_t>(tp) * T_pad * H;
   const int64_t rows_x_h = T_pad * H;
   bool direct = false;
@@ -671,15 +680,27 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
              (H <= 1024 && rows_x_h <= (int64_t{1} << 22));
     if (direct && !nvfp4 && tp <= 4 && rows_x_h >= (int64_t{1} << 18) && rows_x_h <= 800000)
       vec = 2;
+    if (direct && H > 3072 && tp >= 2) {
+      if (T_pad <= 16 || (!nvfp4 && (T_pad <= 24 || (tp <= 5 && T_pad <= 32))))
+        split = 4;
+      else if (!nvfp4 && tp <= 5 && T_pad <= 48)
+        split = 8;
+    }
     if (!direct && H >= 3072 && T_pad <= 4 * kSmsHint)
       one_round = static_cast<int>((T_pad + kSmsHint - 1) / kSmsHint);
   } else if (H <= 8192) {
+    const bool mid_h = H <= 5120;                     // H 4097-5120
+    const bool mid_h_nv = mid_h && (!nvfp4 || H > 4608);  // NVFP4 only from H 4609
     if (tp <= 5) {
-      split = (tp >= 2 && H >= 6144 && T_pad <= 16) ? 8 : 0;
+      split = (tp >= 2 && T_pad <= 16) ? ((H >= 6144 || !nvfp4) ? 8 : 4) : 0;
     } else if (tp < 12) {
       split = T_pad <= 12 ? 8 : (T_pad <= 64 ? ((H >= 6144 || T_pad <= 32) ? 4 : 2) : 0);
+      if (mid_h_nv && T_pad > 64 && T_pad <= 96) split = 4;
     } else {
       split = T_pad <= 16 ? (H >= 7168 ? 8 : 4) : (T_pad <= 64 ? 4 : 0);
+      if (mid_h && !nvfp4 && T_pad > 32 && T_pad <= 64) split = 2;
+      if (T_pad > 64 && ((mid_h_nv && T_pad <= 96) || (H >= 7168 && T_pad <= 80))) split = 4;
+      if (mid_h_nv && nvfp4 && T_pad > 96 && T_pad <= 128) split = 4;
     }
     if (split) {
       direct = true;
@@ -701,17 +722,17 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     if (!direct && !ring_1 && H <= 6144 && T_pad > kSmsHint && T_pad <= 4 * kSmsHint)
       one_round = static_cast<int>((T_pad + kSmsHint - 1) / kSmsHint);
   } else {
-    split = tp < 2                      ? 0
-          : T_pad <= (tp <= 5 ? 16 : 24) ? 8
-          : T_pad <= 64                   ? 4
-          : (T_pad <= 80 && H <= 12288)   ? 8
-                                          : 0;
+    split = tp < 2                                ? 0
+          : T_pad <= (tp <= 5 ? 16 : 24)           ? 8
+          : T_pad <= 64                             ? ((H > 12288 && tp <= 5) ? 8 : 4)
+          : (T_pad <= 80 && H <= 12288)             ? 8
+                                                    : 0;
     direct = split > 0 || (tp <= 5 && (T_pad <= 96 || (T_pad <= 128 && H <= 12288)));
   }
   if (direct) {
     c.kernel = SP_KERNEL_DIRECT;
     c.vec_per_thread = split > 0 ? 1 : (vec ? vec : (H <= 4096 ? 1 : (H <= 8192 ? 2 : 4)));
-    c.ctas_per_sm = H <= 4096 ? 16 : 8;
+    c.ctas_per_sm = (H <= 4096 && split == 0) ? 16 : 8;
     c.stages = 0;
     c.split = split;
   } else if (ring_1 && c.kernel == SP_KERNEL_STAGED && max_stages(H, 1) >= c.stages) {

@@ -107,7 +107,14 @@ def test_launch_selection(lib):
     (8, 512, 2048, (1, 1, 16, 0)),
     (4, 4096, 1024, (1, 1, 16, 0)),
     (4, 8192, 1024, (0, 2, 16, 4)),
-    (8, 8, 4096, (1, 1, 16, 0)),        # never split at H <= 4096
+    (8, 16, 3072, (1, 1, 16, 0)),       # no split up to H = 3072
+    # 3072 < H <= 4096: split 4 up to 16 rows (24 rows, 32 at tp <= 5), split 8 up to 48 rows at
+    # tp <= 5 (the longer bands not for NVFP4)
+    (8, 8, 4096, (1, 1, 8, 0, 4)),
+    (8, 24, 4096, (1, 1, 8, 0, 4)),
+    (8, 32, 4096, (1, 1, 16, 0)),
+    (4, 32, 4096, (1, 1, 8, 0, 4)),
+    (4, 48, 4096, (1, 1, 8, 0, 8)),
     # ... two at tp <= 4 for 2^18 <= T * H <= 800 K, and up to 1.4 M (tp <= 4) / 1.2 M (tp <= 8)
     (4, 64, 4096, (1, 2, 16, 0)),
     (4, 128, 4096, (1, 2, 16, 0)),
@@ -127,17 +134,20 @@ def test_launch_selection(lib):
     (16, 16, 7168, (1, 1, 8, 0, 8)),
     (16, 64, 8192, (1, 1, 8, 0, 4)),
     (2, 8, 7168, (1, 1, 8, 0, 8)),
-    (4, 8, 5120, (1, 2, 8, 0)),         # tp <= 5 splits from H = 6144
+    (4, 8, 5120, (1, 1, 8, 0, 8)),      # tp <= 5: 8 per row up to 16 rows (NVFP4 below 6144: 4)
+    (4, 32, 5120, (1, 2, 8, 0)),
     (4, 16, 8192, (1, 1, 8, 0, 8)),
     (1, 8, 8192, (1, 2, 8, 0)),         # a single partial: no split
     # then direct, two vectors per thread, up to 128 rows (tp >= 12: 96, or 128 below 7168)
     (4, 32, 8192, (1, 2, 8, 0)),
     (4, 64, 8192, (1, 2, 8, 0)),
-    (8, 72, 5120, (1, 2, 8, 0)),
+    (8, 72, 5120, (1, 1, 8, 0, 4)),     # 65-96 rows at H <= 5120, tp >= 6: 4 per row
+    (12, 96, 5120, (1, 1, 8, 0, 4)),
+    (16, 48, 5120, (1, 1, 8, 0, 2)),    # tp >= 12, 33-64 rows at H <= 5120: 2 per row
     (8, 72, 8192, (1, 2, 8, 0)),
     (4, 128, 7168, (1, 2, 8, 0)),
     (2, 160, 8192, (1, 2, 8, 0)),       # tp <= 3 at H >= 7168: up to 160 rows
-    (16, 80, 8192, (1, 2, 8, 0)),
+    (16, 80, 8192, (1, 1, 8, 0, 4)),    # tp >= 12, 65-96 rows at H >= 7168: 4 per row
     (16, 112, 5120, (1, 2, 8, 0)),
     (16, 112, 8192, (0, 2, 1, 0)),      # tp >= 12, 97-128 rows at H = 8192: deep ring, 1/SM
     (16, 112, 7168, (1, 2, 8, 0)),
@@ -153,7 +163,7 @@ def test_launch_selection(lib):
     (4, 384, 7168, (0, 2, 2, 4)),       # ... but not at tp = 4
     # H > 8192: split rows, else (tp <= 5) direct with four vectors per thread, for few rows
     (2, 16, 16384, (1, 1, 8, 0, 8)),
-    (2, 32, 16384, (1, 1, 8, 0, 4)),
+    (2, 32, 16384, (1, 1, 8, 0, 8)),    # H > 12288, tp <= 5: 8 per row up to 64 rows
     (8, 24, 16384, (1, 1, 8, 0, 8)),
     (4, 32, 12288, (1, 1, 8, 0, 4)),
     (4, 64, 12288, (1, 1, 8, 0, 4)),
@@ -175,6 +185,29 @@ def test_launch_rule(lib, tp, T, H, want):
     c = sp.sp_select_launch(tp, T, H, "none")
     want = tuple(want) + (0,) * (5 - len(want))
     assert (c.kernel, c.vec_per_thread, c.ctas_per_sm, c.stages, c.split) == want
+
+
+@pytest.mark.parametrize("mode,tp,T,H,split", [
+    # NVFP4 output: split 4 (not 8) for few rows below H = 6144, and the longer split bands only
+    # from H = 4609 (at H = 4608 a split lost there); per-token FP8 follows bf16
+    ("nvfp4", 4, 8, 5120, 4),
+    ("fp8_per_token", 4, 8, 5120, 8),
+    ("nvfp4", 8, 8, 4096, 4),
+    ("nvfp4", 4, 32, 4096, 0),
+    ("fp8_per_token", 4, 32, 4096, 4),
+    ("nvfp4", 8, 96, 4608, 0),
+    ("fp8_per_token", 8, 96, 4608, 4),
+    ("nvfp4", 12, 96, 5120, 4),
+    ("nvfp4", 16, 112, 5120, 4),
+    ("fp8_per_token", 16, 112, 5120, 0),
+    ("nvfp4", 16, 48, 5120, 4),
+    ("fp8_per_token", 16, 48, 5120, 2),
+])
+def test_launch_rule_by_mode(lib, mode, tp, T, H, split):
+    c = sp.sp_select_launch(tp, T, H, mode)
+    assert c.split == split
+    if split:
+        assert (c.kernel, c.vec_per_thread, c.ctas_per_sm) == (1, 1, 8)
 
 
 A = 1 << 20  # fake 16-byte-aligned addresses: compared, never dereferenced

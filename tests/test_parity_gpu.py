@@ -635,8 +635,16 @@ def test_dynamic_schedule_soak_two_chained_streams():
     (8, 48, 5120, "fp8_per_token", (1, 1, 8, 0, 2)),  # split rows, 2 CTAs per row
     (8, 192, 5120, "nvfp4", (1, 1, 8, 0, 2)),         # split 2 up to 224 rows at H = 5120
     (6, 156, 6144, "fp8_static", (1, 1, 8, 0, 4)),    # split 4 up to 160 rows at H = 6144
-    (16, 96, 5120, "nvfp4", (1, 2, 8, 0)),            # direct up to 128 rows below H = 7168
-    (2, 24, 16384, "fp8_static", (1, 1, 8, 0, 4)),    # split rows at H > 8192, tp <= 5
+    (16, 96, 5120, "nvfp4", (1, 1, 8, 0, 4)),         # split 4 for 65-128 rows, tp >= 12
+    (16, 112, 5120, "fp8_static", (1, 2, 8, 0)),      # direct up to 128 rows below H = 7168
+    (8, 16, 4096, "fp8_per_token", (1, 1, 8, 0, 4)),  # split 4 above H = 3072
+    (4, 48, 4096, "none", (1, 1, 8, 0, 8)),           # split 8 up to 48 rows at tp <= 5
+    (4, 8, 5120, "nvfp4", (1, 1, 8, 0, 4)),           # tp <= 5, NVFP4 below H = 6144
+    (8, 80, 5120, "none", (1, 1, 8, 0, 4)),           # 65-96 rows at H <= 5120, tp >= 6
+    (16, 48, 5120, "fp8_per_token", (1, 1, 8, 0, 2)), # 33-64 rows at H <= 5120, tp >= 12
+    (12, 72, 7168, "none", (1, 1, 8, 0, 4)),          # 65-96 rows at H >= 7168, tp >= 12
+    (4, 40, 16384, "fp8_per_token", (1, 1, 8, 0, 8)), # split 8 up to 64 rows above H = 12288
+    (2, 24, 12288, "fp8_static", (1, 1, 8, 0, 4)),    # split rows at H > 8192, tp <= 5
     (4, 96, 16384, "nvfp4", (1, 4, 8, 0)),            # direct, four vectors per thread
     (16, 48, 12288, "nvfp4", (1, 1, 8, 0, 4)),        # split rows at H > 8192
     (8, 80, 12288, "fp8_per_token", (1, 1, 8, 0, 8)), # 8 CTAs per row up to 80 rows
