@@ -654,17 +654,24 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   //                     up to 128 rows). Then direct with two vectors per thread up to 128 rows (160 at
   //                     tp <= 3 and H >= 7168; at tp >= 12 up to 96, or 128 below H = 8192:
   //                     15-36 % faster than the one-CTA-per-SM deep ring it replaced), split 2 up
-  //                     to 224 rows at H = 5120 and split 4 up to 160 at H = 6144 (tp < 12); the
-  //                     deep ring at one CTA per SM for tp >= 12 and 97-128 rows at H = 8192; one
-  //                     round of rows for H <= 6144 (17-41 % faster at H = 6144, T = 320-384);
+  //                     to 224 rows at H = 5120, and at H 5121-6144 (tp < 12) split 2 up to 152
+  //                     rows (NVFP4: 4) and 4 up to 160; at H >= 7168, 129-144 rows split 4 for
+  //                     4 <= tp < 12 (tp <= 5: 2 for 145-152 rows and 4 up to 160); the deep ring
+  //                     at one CTA per SM for tp >= 12 and 97-128 rows at H = 8192, then split 4
+  //                     for 129-144 rows (up to 160 at H <= 6144); one round of rows for
+  //                     H <= 6144 (17-41 % faster at H = 6144, T = 320-384);
   //   H > 8192:         split rows (tp >= 2): 8 CTAs per row up to 16 rows (24 at tp >= 6), 4 up
   //                     to 64 (8 above H = 12288 at tp <= 5), 8 up to 80 at H <= 12288 (16-36 %
-  //                     faster); then at tp <= 5 direct with four vectors per thread up to 96
+  //                     faster) and for 153-160 rows, just past one round of the one-CTA-per-SM
+  //                     ring; then at tp <= 5 direct with four vectors per thread up to 96
   //                     rows (128 at H <= 12288); else staged.
   // The split bands were widened once the split kernel combined a row's sums with asynchronous
   // pushes instead of a cluster barrier per row: over 796 shapes swept again (tp 2-16, H 2048-
   // 16384, T 8-128, bf16, per-token FP8 and NVFP4 output) the new bands are 2.1 % faster summed
-  // (up to 24 % on one shape: tp 16, H 5120, 96 rows) and slower on none by more than 1 %.
+  // (up to 24 % on one shape: tp 16, H 5120, 96 rows) and slower on none by more than 1 %. A
+  // second sweep of 456 shapes around one round of rows (T 112-256, H 4096-16384, tp 2-16, the
+  // three output kinds) found the staged ring 25-45 % slower than split rows at 129-144 rows and
+  // H >= 7168: the bands for 129-160 rows come from it (4.9 % faster summed, none slower).
   const int64_t elems = static_cast<int64_t>(tp) * T_pad * H;
   const int64_t rows_x_h = T_pad * H;
   bool direct = false;
@@ -712,12 +719,18 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
         split = 2;
       } else if (H <= 6144 && T_pad <= 160) {
         direct = true;
-        split = 4;
+        split = (T_pad <= 152 && !nvfp4) ? 2 : 4;
+      } else if (H >= 7168 && tp >= 4 && T_pad <= (tp <= 5 ? 160 : 144)) {
+        direct = true;
+        split = (T_pad > 144 && T_pad <= 152) ? 2 : 4;
       }
     } else if (T_pad <= 96 || (T_pad <= 128 && H < 8192)) {
       direct = true;
     } else if (T_pad <= 128) {
       ring_1 = true;
+    } else if (T_pad <= 144 || (H <= 6144 && T_pad <= 160)) {
+      direct = true;
+      split = 4;
     }
     if (!direct && !ring_1 && H <= 6144 && T_pad > kSmsHint && T_pad <= 4 * kSmsHint)
       one_round = static_cast<int>((T_pad + kSmsHint - 1) / kSmsHint);
@@ -726,6 +739,7 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
           : T_pad <= (tp <= 5 ? 16 : 24)           ? 8
           : T_pad <= 64                             ? ((H > 12288 && tp <= 5) ? 8 : 4)
           : (T_pad <= 80 && H <= 12288)             ? 8
+          : (H <= 12288 && T_pad > 152 && T_pad <= 160) ? 8
                                                     : 0;
     direct = split > 0 || (tp <= 5 && (T_pad <= 96 || (T_pad <= 128 && H <= 12288)));
   }

@@ -157,7 +157,14 @@ def test_launch_selection(lib):
     (8, 384, 5120, (0, 2, 3, 0)),
     (6, 384, 6144, (0, 2, 3, 0)),
     (8, 512, 5120, (0, 2, 2, 0)),       # 1.1 rounds at 3 CTAs/SM: 2 CTAs/SM fill the last one
-    (16, 144, 8192, (0, 2, 2, 4)),
+    (16, 144, 8192, (1, 1, 8, 0, 4)),   # tp >= 12, 129-144 rows: 4 per row
+    (16, 160, 6144, (1, 1, 8, 0, 4)),   # ... and up to 160 rows at H <= 6144
+    (16, 160, 8192, (0, 2, 2, 4)),
+    (8, 144, 8192, (1, 1, 8, 0, 4)),    # H >= 7168, tp >= 4, 129-144 rows: 4 per row
+    (4, 152, 8192, (1, 1, 8, 0, 2)),    # ... 2 per row for 145-152 at tp <= 5
+    (4, 160, 7168, (1, 1, 8, 0, 4)),    # ... and 4 again up to 160 rows at tp <= 5
+    (8, 152, 6144, (1, 1, 8, 0, 2)),    # H 5121-6144: 2 per row up to 152 rows
+    (8, 160, 12288, (1, 1, 8, 0, 8)),   # H 8193-12288, 153-160 rows: 8 per row
     (16, 256, 7168, (0, 2, 2, 4)),
     (8, 384, 7168, (0, 2, 1, 0)),       # 1.3 rounds at 2 CTAs/SM; long rows: one CTA per SM
     (4, 384, 7168, (0, 2, 2, 4)),       # ... but not at tp = 4

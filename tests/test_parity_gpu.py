@@ -644,6 +644,11 @@ def test_dynamic_schedule_soak_two_chained_streams():
     (16, 48, 5120, "fp8_per_token", (1, 1, 8, 0, 2)), # 33-64 rows at H <= 5120, tp >= 12
     (12, 72, 7168, "none", (1, 1, 8, 0, 4)),          # 65-96 rows at H >= 7168, tp >= 12
     (4, 40, 16384, "fp8_per_token", (1, 1, 8, 0, 8)), # split 8 up to 64 rows above H = 12288
+    (8, 144, 8192, "fp8_per_token", (1, 1, 8, 0, 4)), # 129-144 rows at H >= 7168: split 4
+    (4, 152, 7168, "nvfp4", (1, 1, 8, 0, 2)),         # 145-152 rows at tp <= 5: split 2
+    (16, 144, 5120, "none", (1, 1, 8, 0, 4)),         # tp >= 12, 129-144 rows: split 4
+    (8, 152, 6144, "none", (1, 1, 8, 0, 2)),          # H 5121-6144, up to 152 rows: split 2
+    (8, 160, 12288, "fp8_static", (1, 1, 8, 0, 8)),   # 153-160 rows at H <= 12288: split 8
     (2, 24, 12288, "fp8_static", (1, 1, 8, 0, 4)),    # split rows at H > 8192, tp <= 5
     (4, 96, 16384, "nvfp4", (1, 4, 8, 0)),            # direct, four vectors per thread
     (16, 48, 12288, "nvfp4", (1, 1, 8, 0, 4)),        # split rows at H > 8192
