@@ -178,7 +178,7 @@ VARIANTS = {
 # (workload, variant) pairs measured beside the other workloads
 # Decode-sized calls (tp, tokens, H) of the per-token FP8 workload's kind: latency-bound, so each
 # is also timed replayed from a CUDA graph.
-DECODE_RUNS = [(8, 8, 8192), (8, 64, 8192), (8, 256, 8192)]
+DECODE_RUNS = [(8, 8, 8192), (8, 64, 8192), (8, 256, 8192), (8, 16, 4096), (8, 144, 8192)]
 
 VARIANT_RUNS = [("tp4_T4093p4096_H4096_bf16", "first"),
                 ("tp4_T4093p4096_H4096_bf16", "scaled_addend"),
