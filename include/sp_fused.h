@@ -292,20 +292,26 @@ sp_status sp_fused_reduce_norm_noalloc(const void* partials, int tp, int64_t T_p
  *   kernel        SP_KERNEL_STAGED: one CTA per row at a time; a producer thread streams the
  *                 row's tp partial rows and residual row from HBM into a shared-memory ring with
  *                 bulk asynchronous copies (cp.async.bulk + mbarrier), consumer warps reduce
- *                 from shared memory. SP_KERNEL_DIRECT: the same CTA-per-row mapping with
- *                 128-bit loads straight into registers.
+ *                 from shared memory. With split > 1 (one vector per thread): one cluster of
+ *                 `split` CTAs per row, every row at once (grid = split x T rows), each CTA
+ *                 bringing its slice of all the row's segments into shared memory with one bulk
+ *                 copy each (no ring; stages and ctas_per_sm are ignored); a slice of every
+ *                 segment must fit one CTA's shared memory (else SP_ERR_UNSUPPORTED).
+ *                 SP_KERNEL_DIRECT: the same CTA-per-row mapping with 128-bit loads straight into
+ *                 registers.
  *   vec_per_thread  16-byte vectors (8 elements) of a row that each consumer thread owns: 1, 2, 4.
  *   ctas_per_sm     CTAs per SM the grid is sized for: grid = SMs x min(ctas_per_sm, CTAs of
  *                   this kernel an SM can hold), capped at T_pad; 1 .. 32.
  *   stages          shared-memory ring depth in row segments of 2*H bytes (STAGED only); 0 picks
  *                   the deepest ring that fits ctas_per_sm CTAs on an SM.
- *   split           CTAs that share each row (DIRECT only, vec_per_thread 1 or 2): 0 or 1, a row
- *                   per CTA; 2, 4 or 8, a thread-block cluster of that many CTAs per row, each
- *                   owning a contiguous slice of it and combining the row's sum of squares (and
- *                   max) through distributed shared memory, so that a call with few rows uses
- *                   `split` times as many SMs. Grid = split x min(T rows, SMs x ctas_per_sm /
- *                   split) CTAs. Another value is SP_ERR_INVALID_ARG; split > 1 with the STAGED
- *                   kernel or vec_per_thread 4 is SP_ERR_UNSUPPORTED.
+ *   split           CTAs that share each row: 0 or 1, a row per CTA; 2, 4 or 8, a thread-block
+ *                   cluster of that many CTAs per row, each owning a contiguous slice of it and
+ *                   combining the row's sum of squares (and max) through distributed shared
+ *                   memory, so that a call with few rows uses `split` times as many SMs. DIRECT
+ *                   (vec_per_thread 1 or 2): grid = split x min(T rows, SMs x ctas_per_sm /
+ *                   split) CTAs; STAGED (vec_per_thread 1): see above. Another value is
+ *                   SP_ERR_INVALID_ARG; split > 1 with vec_per_thread 4, or with the STAGED kernel
+ *                   at vec_per_thread 2, is SP_ERR_UNSUPPORTED.
  * Launch shapes are this library's choice for GB300 and have no counterpart on the pages (their
  * fused operators are Ascend kernels); the function computed is sp_fused_reduce_norm's.
  */

@@ -132,6 +132,7 @@ struct DeviceInfo {
   std::atomic<int> sms{0};
   std::atomic<bool> staged_attr_set[3][4][2] = {};
   std::atomic<bool> fc2_attr_set{false};
+  std::atomic<bool> slice_attr_set[4][3] = {};  // [quant mode][split 2, 4, 8]
   // Row counter slots of the dynamic schedule: slot i belongs to the stream with id slot_stream[i];
   // `counters` is the device address of the table (spk::g_row_counters) in this device's context.
   unsigned int* counters = nullptr;
@@ -415,9 +416,59 @@ cudaError_t launch_direct_batched(const sp_launch_config& cfg, spk::Params& p,
   return launch_direct<kVec, kMode, kSplit, 4>(cfg, p, stream, dev);
 }
 
+// Split rows through shared memory (k_slice): one cluster of `split` CTAs per row, every row at
+// once (grid = rows x split); each CTA holds its slice of the row's segments in shared memory.
+int slice_segments(const spk::Params& p) {
+  return p.tp + (p.residual ? 1 : 0) + (p.addend ? 1 : 0);
+}
+int slice_smem_bytes(const spk::Params& p) { return slice_segments(p) * p.split_chunk * 16; }
+// Dynamic shared memory k_slice may take: the per-CTA limit less room for its static arrays.
+constexpr int kSliceSmemMax = kSmemPerCtaMax - 4096;
+
+template <int kMode, int kSplit>
+cudaError_t launch_slice(const spk::Params& p, cudaStream_t stream, DeviceInfo* dev) {
+  auto kernel = spk::k_slice<kMode, kSplit>;
+  const int smem = slice_smem_bytes(p);
+  cudaError_t e = cudaSuccess;
+  std::atomic<bool>& attr_set =
+      dev->slice_attr_set[kMode][kSplit == 2 ? 0 : (kSplit == 4 ? 1 : 2)];
+  if (!attr_set.load(std::memory_order_acquire)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSliceSmemMax);
+    if (e != cudaSuccess) return e;
+    attr_set.store(true, std::memory_order_release);
+  }
+  cudaLaunchConfig_t lc{};
+  lc.gridDim = dim3(static_cast<unsigned>(p.rows_total * kSplit));
+  lc.blockDim = dim3(static_cast<unsigned>(p.nthreads));
+  lc.dynamicSmemBytes = static_cast<size_t>(smem);
+  lc.stream = stream;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kSplit;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 2;
+  t_last_launch.grid = static_cast<int>(p.rows_total * kSplit);
+  e = cudaLaunchKernelEx(&lc, kernel, p);
+  return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 template <int kVec, int kMode>
 cudaError_t launch_one(const sp_launch_config& cfg, spk::Params& p, int smem, const Extras& x,
                        cudaStream_t stream, DeviceInfo* dev) {
+  if constexpr (kVec == 1) {
+    if (cfg.kernel == SP_KERNEL_STAGED && x.withhold < 0) {
+      switch (split_of(cfg)) {
+        case 2: return launch_slice<kMode, 2>(p, stream, dev);
+        case 4: return launch_slice<kMode, 4>(p, stream, dev);
+        case 8: return launch_slice<kMode, 8>(p, stream, dev);
+        default: break;
+      }
+    }
+  }
   int grid = 0;
   const int schedule = x.schedule;
   if (cfg.kernel == SP_KERNEL_DIRECT) {
@@ -501,12 +552,13 @@ sp_status config_is_valid(const sp_launch_config& cfg, int64_t H) {
   if (cfg.split != 0 && cfg.split != 1 && cfg.split != 2 && cfg.split != 4 && cfg.split != 8)
     return SP_ERR_INVALID_ARG;
   const int split = split_of(cfg);
-  if (split > 1 && (cfg.kernel != SP_KERNEL_DIRECT || cfg.vec_per_thread > 2))
+  if (split > 1 && (cfg.vec_per_thread > 2 ||
+                    (cfg.kernel == SP_KERNEL_STAGED && cfg.vec_per_thread != 1)))
     return SP_ERR_UNSUPPORTED;
   const int threads = split > 1 ? split_threads(H, split, cfg.vec_per_thread)
                                 : consumer_threads(H, cfg.vec_per_thread);
   if (threads > spk::kMaxConsumerThreads) return SP_ERR_UNSUPPORTED;
-  if (cfg.kernel == SP_KERNEL_STAGED) {
+  if (cfg.kernel == SP_KERNEL_STAGED && split <= 1) {
     const int most = max_stages(H, cfg.ctas_per_sm);
     if (cfg.stages < 0 || cfg.stages > most || most < 2 || cfg.stages == 1)
       return SP_ERR_UNSUPPORTED;
@@ -558,7 +610,10 @@ sp_status run_checked(const sp_launch_config& cfg_in, const void* partials, int 
   p.wait_limit_ns = x.wait_limit_ns;
   p.withhold = x.withhold;
   int smem = 0;
-  if (cfg.kernel == SP_KERNEL_STAGED) {
+  if (cfg.kernel == SP_KERNEL_STAGED && split_of(cfg) > 1 &&
+      slice_smem_bytes(p) > kSliceSmemMax)  // its row slices do not fit one CTA
+    return SP_ERR_UNSUPPORTED;
+  if (cfg.kernel == SP_KERNEL_STAGED && split_of(cfg) <= 1) {
     if (cfg.stages == 0) cfg.stages = max_stages(H, cfg.ctas_per_sm);
     p.stages = cfg.stages;
     p.seg_stride = seg_stride(H);
@@ -672,6 +727,14 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   // second sweep of 456 shapes around one round of rows (T 112-256, H 4096-16384, tp 2-16, the
   // three output kinds) found the staged ring 25-45 % slower than split rows at 129-144 rows and
   // H >= 7168: the bands for 129-160 rows come from it (4.9 % faster summed, none slower).
+  // Staged split rows (k_slice: a cluster per row, the row's slices held in shared memory) then
+  // take the calls just past what the direct split kernel covers in one round: 4 CTAs per row at
+  // H = 3073-4096 for 145-192 rows at tp >= 12 and, for NVFP4, 161-256 rows at tp 6-11; at
+  // H >= 7168 for 145-160 rows at tp 6-11 and 161-192 rows at tp <= 5. Over 195 swept shapes
+  // (tp 2-16, H 4096-16384, T 16-320) 1.5 % faster summed, none slower; against the previous
+  // rule 8-38 % faster on L2-resident inputs (tp 8, H 8192, 160 rows: 8.31 -> 5.18 µs); on
+  // inputs from HBM 7-37 % faster at H = 4096, -9 to +1 % at tp 8 and H >= 7168, and 4-11 %
+  // slower at tp <= 5.
   const int64_t elems = static_cast<int64_t>(tp) * T_pad * H;
   const int64_t rows_x_h = T_pad * H;
   bool direct = false;
@@ -679,6 +742,7 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   int one_round = 0;    // staged at this many CTAs per SM with the deepest ring
   int vec = 0;          // direct kernel: vectors per thread (0: by H)
   int split = 0;
+  int slice = 0;  // the staged kernel's split-row form (k_slice), this many CTAs per row
   const bool nvfp4 = quant_mode == SP_QUANT_NVFP4;
   if (H <= 4096) {
     direct = (rows_x_h <= (int64_t{1} << 20) && (tp < 12 || H < 3072 || elems <= 12600000)) ||
@@ -695,6 +759,9 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     }
     if (!direct && H >= 3072 && T_pad <= 4 * kSmsHint)
       one_round = static_cast<int>((T_pad + kSmsHint - 1) / kSmsHint);
+    if (H > 3072 && ((tp >= 12 && T_pad > 144 && T_pad <= 192) ||
+                     (nvfp4 && tp >= 6 && tp < 12 && T_pad > 160 && T_pad <= 256)))
+      slice = 4;
   } else if (H <= 8192) {
     const bool mid_h = H <= 5120;                     // H 4097-5120
     const bool mid_h_nv = mid_h && (!nvfp4 || H > 4608);  // NVFP4 only from H 4609
@@ -734,6 +801,9 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     }
     if (!direct && !ring_1 && H <= 6144 && T_pad > kSmsHint && T_pad <= 4 * kSmsHint)
       one_round = static_cast<int>((T_pad + kSmsHint - 1) / kSmsHint);
+    if (H >= 7168 && ((tp <= 5 && T_pad > 160 && T_pad <= 192) ||
+                      (tp >= 6 && tp < 12 && T_pad > 144 && T_pad <= 160)))
+      slice = 4;
   } else {
     split = tp < 2                                ? 0
           : T_pad <= (tp <= 5 ? 16 : 24)           ? 8
@@ -743,7 +813,13 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
                                                     : 0;
     direct = split > 0 || (tp <= 5 && (T_pad <= 96 || (T_pad <= 128 && H <= 12288)));
   }
-  if (direct) {
+  if (slice) {
+    c.kernel = SP_KERNEL_STAGED;
+    c.vec_per_thread = 1;
+    c.ctas_per_sm = 8;
+    c.stages = 0;
+    c.split = slice;
+  } else if (direct) {
     c.kernel = SP_KERNEL_DIRECT;
     c.vec_per_thread = split > 0 ? 1 : (vec ? vec : (H <= 4096 ? 1 : (H <= 8192 ? 2 : 4)));
     c.ctas_per_sm = (H <= 4096 && split == 0) ? 16 : 8;

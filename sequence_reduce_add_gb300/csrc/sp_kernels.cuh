@@ -451,6 +451,79 @@ __global__ void __launch_bounds__(kMaxConsumerThreads) k_direct(const Params p) 
   }
 }
 
+// ------------------------------------------------------------------------------------ slice
+// The staged kernel's split-row form: one row per cluster of kSplit CTAs (cluster b takes row
+// b), CTA r owning vectors [r * split_chunk, (r + 1) * split_chunk) of the row as in k_direct's
+// split variant. The CTA brings its slice of every segment of the row (the tp partials, the
+// residual, the addend) into shared memory with one bulk asynchronous copy each, all in flight at
+// once and none held in registers, then adds them, and the cluster combines the row's sums as
+// k_direct's split rows do (cluster_row_sum). A call whose rows' slices all fit on the SMs at once
+// then costs one round trip to memory per row and draws on every SM.
+template <int kMode, int kSplit>
+__global__ void __launch_bounds__(kMaxConsumerThreads) k_slice(const Params p) {
+  static_assert(kSplit >= 2 && kSplit <= 8, "a cluster of 2 to 8 CTAs per row");
+  extern __shared__ __align__(128) unsigned char smem[];  // [segment][slice vector] uint4
+  __shared__ RedSlot slots[64];
+  __shared__ __align__(8) uint64_t loaded;
+  const int c = threadIdx.x;
+  const int64_t H = p.H;
+  const int rank = cluster_rank();
+  const int vbase = rank * p.split_chunk;
+  const int vend = min(vbase + p.split_chunk, p.nvec);
+  const int nv = vend > vbase ? vend - vbase : 0;  // this CTA's vectors of the row
+  const int64_t t = blockIdx.x / kSplit;
+  bool setup_seen = false;
+  if (c == 0) {
+    cluster_exchange_init();
+    mbar_init(smem_addr(&loaded), 1);
+    fence_mbar_init();
+  }
+  cluster_arrive_relaxed();
+  __syncthreads();
+  pdl_launch_dependents();
+  pdl_wait_prerequisites();
+  if (t >= p.T_valid) {  // a padding row (or a row past T_pad of the swizzled scale layout)
+    zero_row<1, kMode, kSplit>(p, t, c, vbase, vend);
+    cluster_wait();  // complete the set-up barrier this CTA arrived at
+    return;
+  }
+  const int nseg = p.tp + (p.residual ? 1 : 0) + (p.addend ? 1 : 0);
+  const uint32_t bar = smem_addr(&loaded);
+  if (c < 32) {
+    if (c == 0) mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nseg * nv) * 16u);
+    if (nv > 0) {
+      const uint64_t policy = l2_evict_first_policy();
+      for (int seg = c; seg < nseg; seg += 32) {
+        const uint16_t* row = seg < p.tp                     ? p.partials + seg * p.plane
+                            : (seg == p.tp && p.residual) ? p.residual
+                                                          : p.addend;
+        bulk_g2s(smem_addr(smem + static_cast<size_t>(seg) * nv * 16), row + t * H + vbase * 8,
+                 static_cast<uint32_t>(nv) * 16u, bar, policy);
+      }
+    }
+  }
+  uint4 w[1], b[1];
+  load_row_constants<1, kSplit>(p, c, w, b, vbase, vend);
+  const QuantConst qc = load_quant_const<kMode>(p);
+  if (!mbar_wait_bounded(bar, 0, nullptr)) {
+    if (c == 0) atomicOr(p.error_word, kErrWaitTimeout);
+    mbar_wait_bounded(bar, 0, nullptr);  // let the copies land before the CTA goes on
+  }
+  float h[1][8];
+#pragma unroll
+  for (int e = 0; e < 8; ++e) h[0][e] = 0.0f;
+  if (c < nv) {
+    const uint4* seg0 = reinterpret_cast<const uint4*>(smem) + c;
+    for (int r = 0; r < p.tp; ++r) add_bf16x8(seg0[r * nv], h[0]);
+    if (p.partial_scale != 1.0f) scale8(h[0], p.partial_scale);
+    int seg = p.tp;
+    if (p.residual) add_bf16x8(seg0[seg++ * nv], h[0]);
+    if (p.addend) add_bf16x8(seg0[seg * nv], h[0]);
+  }
+  add_bf16x8(b[0], h[0]);
+  finish_row<1, kMode, kSplit>(p, t, h, w, qc, slots, 0, c, 0, vbase, vend, rank, &setup_seen, 0);
+}
+
 // ----------------------------------------------------------------------------------- self-test
 // The timeout path of the bounded waits, on the GPU: one warp waits, with the given limit, on an
 // mbarrier that nothing arrives at. The wait must give up, record SP_DEVICE_ERR_WAIT_TIMEOUT in

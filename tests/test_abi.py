@@ -149,6 +149,9 @@ def test_launch_selection(lib):
     (2, 160, 8192, (1, 2, 8, 0)),       # tp <= 3 at H >= 7168: up to 160 rows
     (16, 80, 8192, (1, 1, 8, 0, 4)),    # tp >= 12, 65-96 rows at H >= 7168: 4 per row
     (16, 112, 5120, (1, 2, 8, 0)),
+    (16, 160, 4096, (0, 1, 8, 0, 4)),   # tp >= 12, 145-192 rows at H = 4096: staged split rows
+    (8, 160, 8192, (0, 1, 8, 0, 4)),    # H >= 7168, 6 <= tp < 12, 145-160 rows
+    (4, 192, 8192, (0, 1, 8, 0, 4)),    # H >= 7168, tp <= 5, 161-192 rows
     (16, 112, 8192, (0, 2, 1, 0)),      # tp >= 12, 97-128 rows at H = 8192: deep ring, 1/SM
     (16, 112, 7168, (1, 2, 8, 0)),
     (8, 192, 5120, (1, 1, 8, 0, 2)),    # split 2 up to 224 rows at H = 5120
@@ -207,6 +210,8 @@ def test_launch_rule(lib, tp, T, H, want):
     ("nvfp4", 12, 96, 5120, 4),
     ("nvfp4", 16, 112, 5120, 4),
     ("fp8_per_token", 16, 112, 5120, 0),
+    ("nvfp4", 8, 224, 4096, 4),
+    ("fp8_per_token", 8, 224, 4096, 0),
     ("nvfp4", 16, 48, 5120, 4),
     ("fp8_per_token", 16, 48, 5120, 2),
 ])
@@ -214,7 +219,7 @@ def test_launch_rule_by_mode(lib, mode, tp, T, H, split):
     c = sp.sp_select_launch(tp, T, H, mode)
     assert c.split == split
     if split:
-        assert (c.kernel, c.vec_per_thread, c.ctas_per_sm) == (1, 1, 8)
+        assert (c.vec_per_thread, c.ctas_per_sm) == (1, 8)
 
 
 A = 1 << 20  # fake 16-byte-aligned addresses: compared, never dereferenced

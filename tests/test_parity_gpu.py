@@ -636,7 +636,7 @@ def test_dynamic_schedule_soak_two_chained_streams():
     (8, 192, 5120, "nvfp4", (1, 1, 8, 0, 2)),         # split 2 up to 224 rows at H = 5120
     (6, 156, 6144, "fp8_static", (1, 1, 8, 0, 4)),    # split 4 up to 160 rows at H = 6144
     (16, 96, 5120, "nvfp4", (1, 1, 8, 0, 4)),         # split 4 for 65-128 rows, tp >= 12
-    (16, 112, 5120, "fp8_static", (1, 2, 8, 0)),      # direct up to 128 rows below H = 7168
+    (16, 96, 7168, "fp8_static", (1, 2, 8, 0)),       # direct up to 128 rows below H = 8192
     (8, 16, 4096, "fp8_per_token", (1, 1, 8, 0, 4)),  # split 4 above H = 3072
     (4, 48, 4096, "none", (1, 1, 8, 0, 8)),           # split 8 up to 48 rows at tp <= 5
     (4, 8, 5120, "nvfp4", (1, 1, 8, 0, 4)),           # tp <= 5, NVFP4 below H = 6144
@@ -649,6 +649,10 @@ def test_dynamic_schedule_soak_two_chained_streams():
     (16, 144, 5120, "none", (1, 1, 8, 0, 4)),         # tp >= 12, 129-144 rows: split 4
     (8, 152, 6144, "none", (1, 1, 8, 0, 2)),          # H 5121-6144, up to 152 rows: split 2
     (8, 160, 12288, "fp8_static", (1, 1, 8, 0, 8)),   # 153-160 rows at H <= 12288: split 8
+    (16, 160, 4096, "nvfp4", (0, 1, 8, 0, 4)),        # staged split rows: tp >= 12, H = 4096
+    (8, 224, 4096, "nvfp4", (0, 1, 8, 0, 4)),         # ... NVFP4 at tp 6-11 up to 256 rows
+    (8, 160, 7168, "none", (0, 1, 8, 0, 4)),          # ... H >= 7168, 145-160 rows at tp 6-11
+    (4, 192, 8192, "fp8_static", (0, 1, 8, 0, 4)),    # ... H >= 7168, 161-192 rows at tp <= 5
     (2, 24, 12288, "fp8_static", (1, 1, 8, 0, 4)),    # split rows at H > 8192, tp <= 5
     (4, 96, 16384, "nvfp4", (1, 4, 8, 0)),            # direct, four vectors per thread
     (16, 48, 12288, "nvfp4", (1, 1, 8, 0, 4)),        # split rows at H > 8192
@@ -765,6 +769,80 @@ def test_split_rows_on_host_buffers(mode):
     for k in ("out", "out_scales", "residual_out"):
         assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
     compare(a, run_oracle(inp, scale_layout=layout), inp)
+
+
+# ------------------------------------------------------------------------- staged split rows
+def _slice_cfg(split):
+    return dict(kernel=0, vec_per_thread=1, ctas_per_sm=8, stages=0, split=split)
+
+
+@pytest.mark.parametrize("mode", ["none", "fp8_static", "fp8_per_token", "nvfp4"])
+@pytest.mark.parametrize("split", [2, 4, 8])
+@pytest.mark.parametrize("tp,T,H", [(8, 16, 8192), (4, 40, 4096), (3, 24, 1040), (2, 10, 16),
+                                    (16, 160, 4096)])
+def test_slice_rows(mode, split, tp, T, H):
+    """The staged kernel's split-row form: each CTA of a row's cluster brings its slice of the
+    row's segments into shared memory with one bulk copy each. Every slice size, including CTAs
+    whose slice is empty (H = 16 at split 8) and slices that end mid-warp (H = 1040)."""
+    w = dict(synth.workload(3), mode=mode, scale=0.05 if mode == "fp8_static" else None)
+    inp = synth.make_inputs(w, device=DEV, tp=tp, T_pad=T, T_valid=T - 3, H=H)
+    assert _check(inp, config=_slice_cfg(split))
+
+
+@pytest.mark.parametrize("mode", ["fp8_per_token", "nvfp4"])
+@pytest.mark.parametrize("tp,T_pad,T_valid,layout", [(1, 8, 8, 0), (4, 16, 0, 0), (4, 16, 0, 1),
+                                                     (1, 1, 1, 1), (2, 130, 127, 1)])
+def test_slice_rows_edge_cases(mode, tp, T_pad, T_valid, layout):
+    """Staged split rows at tp = 1, with every row padding (only zeros written, scales
+    included), with a single row, and with the swizzled layout's padding rows beyond T_pad."""
+    if layout and mode != "nvfp4":
+        pytest.skip("the swizzled layout is NVFP4-only")
+    w = dict(synth.workload(3), mode=mode, scale=None)
+    inp = synth.make_inputs(w, device=DEV, tp=tp, T_pad=T_pad, T_valid=T_valid, H=2080)
+    kw = dict(config=_slice_cfg(8), scale_layout=layout)
+    a = run_gpu(inp, fill=0xA5, **kw)
+    b = run_gpu(inp, fill=0x5A, **kw)
+    for k in ("out", "out_scales", "residual_out"):
+        assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+    compare(a, run_oracle(inp, scale_layout=layout), inp)
+
+
+@pytest.mark.parametrize("mode", ["none", "fp8_static", "fp8_per_token", "nvfp4"])
+@pytest.mark.parametrize("split", [2, 8])
+def test_slice_rows_with_options(mode, split):
+    """Staged split rows with a partial scale, an addend (one more segment in shared memory) and
+    (NVFP4) the swizzled scale layout."""
+    w = dict(synth.workload(3), mode=mode, scale=0.05 if mode == "fp8_static" else None)
+    inp = synth.make_inputs(w, device=DEV, tp=4, T_pad=24, T_valid=21, H=1040, with_addend=True)
+    layout = 1 if mode == "nvfp4" else 0
+    kw = dict(config=_slice_cfg(split), partial_scale=0.5, scale_layout=layout)
+    a = run_gpu(inp, fill=0xA5, **kw)
+    b = run_gpu(inp, fill=0x5A, **kw)
+    for k in ("out", "out_scales", "residual_out"):
+        if a[k] is not None:
+            assert np.array_equal(a[k].view(np.uint8), b[k].view(np.uint8)), k
+    compare(a, run_oracle(inp, partial_scale=0.5, scale_layout=layout), inp)
+
+
+@pytest.mark.parametrize("split", [4, 8])
+def test_slice_rows_longest_hidden(split):
+    """Staged split rows at the largest H the kernels take (slices of 256 and 512 vectors, one
+    per thread; two CTAs per row would need 1024 threads and are refused)."""
+    w = dict(synth.workload(3), mode="fp8_per_token", scale=None)
+    inp = synth.make_inputs(w, device=DEV, tp=4, T_pad=12, T_valid=10, H=sp.sp_max_hidden())
+    assert _check(inp, config=_slice_cfg(split))
+
+
+@pytest.mark.parametrize("tp,H,split", [(32, 12288, 2), (4, 16384, 2)])
+def test_slice_rows_refused_when_a_slice_does_not_fit(tp, H, split):
+    """A CTA's slice must fit its shared memory and its threads: 33 segments of 768 vectors
+    (tp = 32, H = 12288, two CTAs per row: 396 KB) and a slice of 1024 vectors (H = 16384, two
+    CTAs per row) are refused before any launch."""
+    w = dict(synth.workload(3), mode="none", scale=None)
+    inp = synth.make_inputs(w, device=DEV, tp=tp, T_pad=tp, T_valid=tp, H=H)
+    with pytest.raises(sp.SpError) as e:
+        run_gpu(inp, config=_slice_cfg(split))
+    assert e.value.status == 2  # SP_ERR_UNSUPPORTED
 
 
 def test_split_rows_on_two_streams_concurrently():
