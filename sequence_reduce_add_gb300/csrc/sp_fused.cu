@@ -730,7 +730,12 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   // Staged split rows (k_slice: a cluster per row, the row's slices held in shared memory) then
   // take the calls just past what the direct split kernel covers in one round: 4 CTAs per row at
   // H = 3073-4096 for 145-192 rows at tp >= 12 and, for NVFP4, 161-256 rows at tp 6-11; at
-  // H >= 7168 for 145-160 rows at tp 6-11 and 161-192 rows at tp <= 5. Over 195 swept shapes
+  // H >= 7168 for 145-160 rows at tp 6-11 and 161-192 rows at tp <= 5. And a few decode bands,
+  // kept where an A/B against direct rows was faster both back to back and from a CUDA graph:
+  // at 4096 < H <= 8192 and tp 2-5, 17-24 rows at H >= 6144 (8 CTAs per row) and 17-32 rows
+  // below (4 per row), 6-21 % faster; NVFP4 at tp >= 12 up to 16 rows and H <= 5120 (4 per row),
+  // 9-13 % faster. (Some other decode shapes that the sweep favoured ran faster from a graph but
+  // 7-43 % slower back to back, and were left out.) Over 195 swept shapes
   // (tp 2-16, H 4096-16384, T 16-320) 1.5 % faster summed, none slower; against the previous
   // rule 8-38 % faster on L2-resident inputs (tp 8, H 8192, 160 rows: 8.31 -> 5.18 µs); on
   // inputs from HBM 7-37 % faster at H = 4096, -9 to +1 % at tp 8 and H >= 7168, and 4-11 %
@@ -760,7 +765,8 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     if (!direct && H >= 3072 && T_pad <= 4 * kSmsHint)
       one_round = static_cast<int>((T_pad + kSmsHint - 1) / kSmsHint);
     if (H > 3072 && ((tp >= 12 && T_pad > 144 && T_pad <= 192) ||
-                     (nvfp4 && tp >= 6 && tp < 12 && T_pad > 160 && T_pad <= 256)))
+                     (nvfp4 && tp >= 6 && tp < 12 && T_pad > 160 && T_pad <= 256) ||
+                     (nvfp4 && tp >= 12 && T_pad <= 16)))
       slice = 4;
   } else if (H <= 8192) {
     const bool mid_h = H <= 5120;                     // H 4097-5120
@@ -804,6 +810,9 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     if (H >= 7168 && ((tp <= 5 && T_pad > 160 && T_pad <= 192) ||
                       (tp >= 6 && tp < 12 && T_pad > 144 && T_pad <= 160)))
       slice = 4;
+    if (tp >= 2 && tp <= 5 && T_pad > 16 && T_pad <= (H >= 6144 ? 24 : 32))
+      slice = H >= 6144 ? 8 : 4;
+    if (nvfp4 && tp >= 12 && T_pad <= 16 && H <= 5120) slice = 4;
   } else {
     split = tp < 2                                ? 0
           : T_pad <= (tp <= 5 ? 16 : 24)           ? 8

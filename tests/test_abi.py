@@ -135,11 +135,13 @@ def test_launch_selection(lib):
     (16, 64, 8192, (1, 1, 8, 0, 4)),
     (2, 8, 7168, (1, 1, 8, 0, 8)),
     (4, 8, 5120, (1, 1, 8, 0, 8)),      # tp <= 5: 8 per row up to 16 rows (NVFP4 below 6144: 4)
-    (4, 32, 5120, (1, 2, 8, 0)),
+    (4, 32, 5120, (0, 1, 8, 0, 4)),     # tp <= 5: staged split rows for 17-32 rows below
+    (4, 24, 8192, (0, 1, 8, 0, 8)),     # H = 6144 (4 per row), 17-24 rows above (8 per row)
     (4, 16, 8192, (1, 1, 8, 0, 8)),
     (1, 8, 8192, (1, 2, 8, 0)),         # a single partial: no split
     # then direct, two vectors per thread, up to 128 rows (tp >= 12: 96, or 128 below 7168)
     (4, 32, 8192, (1, 2, 8, 0)),
+    (4, 40, 8192, (1, 2, 8, 0)),
     (4, 64, 8192, (1, 2, 8, 0)),
     (8, 72, 5120, (1, 1, 8, 0, 4)),     # 65-96 rows at H <= 5120, tp >= 6: 4 per row
     (12, 96, 5120, (1, 1, 8, 0, 4)),

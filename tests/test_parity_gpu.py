@@ -626,7 +626,10 @@ def test_dynamic_schedule_soak_two_chained_streams():
 
 # ------------------------------------------------------------------------- launch-rule bands
 @pytest.mark.parametrize("tp,T,H,mode,band", [
-    (4, 32, 8192, "fp8_per_token", (1, 2, 8, 0)),     # direct, two vectors per thread
+    (4, 48, 8192, "fp8_per_token", (1, 2, 8, 0)),     # direct, two vectors per thread
+    (4, 32, 5120, "fp8_per_token", (0, 1, 8, 0, 4)),  # staged split rows, tp <= 5, 17-32 rows
+    (2, 24, 7168, "none", (0, 1, 8, 0, 8)),           # ... 8 per row for 17-24 rows, H >= 6144
+    (16, 16, 5120, "nvfp4", (0, 1, 8, 0, 4)),         # ... NVFP4, tp >= 12, up to 16 rows
     (4, 128, 4096, "none", (1, 2, 16, 0)),            # direct, two vectors at tp <= 4
     (8, 384, 3072, "fp8_per_token", (1, 1, 16, 0)),   # direct up to 1.2 M at tp <= 8
     (16, 128, 2048, "fp8_static", (1, 1, 16, 0)),     # direct at tp >= 6
