@@ -735,7 +735,12 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   // at 4096 < H <= 8192 and tp 2-5, 17-24 rows at H >= 6144 (8 CTAs per row) and 17-32 rows
   // below (4 per row), 6-21 % faster; NVFP4 at tp >= 12 up to 16 rows and H <= 5120 (4 per row),
   // 9-13 % faster. (Some other decode shapes that the sweep favoured ran faster from a graph but
-  // 7-43 % slower back to back, and were left out.) Over 195 swept shapes
+  // 7-43 % slower back to back, and were left out.) Once the direct and slice kernels let the
+  // next kernel in only at their end, a sweep of 270 shapes around the direct kernel's upper
+  // bound (T 128-512, H 2048-8192) gave two more bands: 4 CTAs per row for 97-128 rows at
+  // 4096 < H <= 5120 and tp >= 6 (3-7 % faster on L2-resident inputs, 4-17 % from HBM), and 2
+  // per row for NVFP4 output past 128 rows in the direct band at H >= 3072 (1-24 % and up to
+  // 38 % faster); the others it suggested were slower on L2-resident inputs and left out. Over 195 swept shapes
   // (tp 2-16, H 4096-16384, T 16-320) 1.5 % faster summed, none slower; against the previous
   // rule 8-38 % faster on L2-resident inputs (tp 8, H 8192, 160 rows: 8.31 -> 5.18 µs); on
   // inputs from HBM 7-37 % faster at H = 4096, -9 to +1 % at tp 8 and H >= 7168, and 4-11 %
@@ -765,9 +770,10 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
     if (!direct && H >= 3072 && T_pad <= 4 * kSmsHint)
       one_round = static_cast<int>((T_pad + kSmsHint - 1) / kSmsHint);
     if (H > 3072 && ((tp >= 12 && T_pad > 144 && T_pad <= 192) ||
-                     (nvfp4 && tp >= 6 && tp < 12 && T_pad > 160 && T_pad <= 256) ||
                      (nvfp4 && tp >= 12 && T_pad <= 16)))
       slice = 4;
+    if (slice == 0 && direct && split == 0 && nvfp4 && tp >= 4 && H >= 3072 && T_pad > 128)
+      slice = 2;
   } else if (H <= 8192) {
     const bool mid_h = H <= 5120;                     // H 4097-5120
     const bool mid_h_nv = mid_h && (!nvfp4 || H > 4608);  // NVFP4 only from H 4609
@@ -812,6 +818,7 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
       slice = 4;
     if (tp >= 2 && tp <= 5 && T_pad > 16 && T_pad <= (H >= 6144 ? 24 : 32))
       slice = H >= 6144 ? 8 : 4;
+    if (tp >= 6 && T_pad > 96 && T_pad <= 128 && H <= 5120) slice = 4;
     if (nvfp4 && tp >= 12 && T_pad <= 16 && H <= 5120) slice = 4;
   } else {
     split = tp < 2                                ? 0
@@ -822,6 +829,8 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
                                                     : 0;
     direct = split > 0 || (tp <= 5 && (T_pad <= 96 || (T_pad <= 128 && H <= 12288)));
   }
+  // a row slice of every segment (the partials, the residual and an addend) must fit one CTA
+  if (slice && static_cast<int64_t>(tp + 2) * split_chunk(H, slice) * 16 > kSliceSmemMax) slice = 0;
   if (slice) {
     c.kernel = SP_KERNEL_STAGED;
     c.vec_per_thread = 1;

@@ -150,7 +150,9 @@ def test_launch_selection(lib):
     (4, 128, 7168, (1, 2, 8, 0)),
     (2, 160, 8192, (1, 2, 8, 0)),       # tp <= 3 at H >= 7168: up to 160 rows
     (16, 80, 8192, (1, 1, 8, 0, 4)),    # tp >= 12, 65-96 rows at H >= 7168: 4 per row
-    (16, 112, 5120, (1, 2, 8, 0)),
+    (16, 112, 5120, (0, 1, 8, 0, 4)),   # 97-128 rows, tp >= 6, H <= 5120: staged split rows
+    (8, 128, 8192, (1, 2, 8, 0)),
+    (16, 320, 2048, (1, 1, 16, 0)),
     (16, 160, 4096, (0, 1, 8, 0, 4)),   # tp >= 12, 145-192 rows at H = 4096: staged split rows
     (8, 160, 8192, (0, 1, 8, 0, 4)),    # H >= 7168, 6 <= tp < 12, 145-160 rows
     (4, 192, 8192, (0, 1, 8, 0, 4)),    # H >= 7168, tp <= 5, 161-192 rows
@@ -211,9 +213,11 @@ def test_launch_rule(lib, tp, T, H, want):
     ("fp8_per_token", 8, 96, 4608, 4),
     ("nvfp4", 12, 96, 5120, 4),
     ("nvfp4", 16, 112, 5120, 4),
-    ("fp8_per_token", 16, 112, 5120, 0),
-    ("nvfp4", 8, 224, 4096, 4),
+    ("fp8_per_token", 16, 112, 5120, 4),
+    ("nvfp4", 8, 224, 4096, 2),         # NVFP4 in the direct band past 128 rows, H >= 3072
     ("fp8_per_token", 8, 224, 4096, 0),
+    ("nvfp4", 4, 192, 3072, 2),
+    ("nvfp4", 16, 192, 4096, 4),
     ("nvfp4", 16, 48, 5120, 4),
     ("fp8_per_token", 16, 48, 5120, 2),
 ])

@@ -653,7 +653,9 @@ def test_dynamic_schedule_soak_two_chained_streams():
     (8, 152, 6144, "none", (1, 1, 8, 0, 2)),          # H 5121-6144, up to 152 rows: split 2
     (8, 160, 12288, "fp8_static", (1, 1, 8, 0, 8)),   # 153-160 rows at H <= 12288: split 8
     (16, 160, 4096, "nvfp4", (0, 1, 8, 0, 4)),        # staged split rows: tp >= 12, H = 4096
-    (8, 224, 4096, "nvfp4", (0, 1, 8, 0, 4)),         # ... NVFP4 at tp 6-11 up to 256 rows
+    (8, 224, 4096, "nvfp4", (0, 1, 8, 0, 2)),         # ... NVFP4 past 128 rows, 2 per row
+    (8, 120, 5120, "fp8_per_token", (0, 1, 8, 0, 4)), # ... 97-128 rows at tp >= 6, H <= 5120
+    (4, 256, 3072, "nvfp4", (0, 1, 8, 0, 2)),         # ... NVFP4 past 128 rows, H = 3072
     (8, 160, 7168, "none", (0, 1, 8, 0, 4)),          # ... H >= 7168, 145-160 rows at tp 6-11
     (4, 192, 8192, "fp8_static", (0, 1, 8, 0, 4)),    # ... H >= 7168, 161-192 rows at tp <= 5
     (2, 24, 12288, "fp8_static", (1, 1, 8, 0, 4)),    # split rows at H > 8192, tp <= 5
