@@ -1,5 +1,5 @@
 """GPU parity on seeded random problems: shapes, modes, optional inputs, options, launch
-configurations (split rows included) and row schedules drawn together, so that combinations the hand-picked cases do not list are
+configurations (split rows of both kernels included) and row schedules drawn together, so that combinations the hand-picked cases do not list are
 covered too. Each problem is compared with the oracle element by element under the tolerances
 of parity_util, after two runs into differently pre-filled, guard-banded outputs. Random
 FlashComm2 reorganisations are compared byte for byte.
@@ -21,6 +21,7 @@ pytestmark = pytest.mark.gpu
 
 DEV = "cuda:0"
 CASES = 128
+SLICE_CASES = 32
 FC2_CASES = 48
 MODES = ["none", "fp8_static", "fp8_per_token", "nvfp4"]
 
@@ -61,6 +62,8 @@ def _draw(i: int) -> dict:
                                stages=r.choice([0, 2, 3, 4]) if kernel == 0 else 0)
             if kernel == 1 and vec <= 2 and r.random() < 0.5:
                 p["config"]["split"] = r.choice([2, 4, 8])
+            elif kernel == 0 and vec == 1 and r.random() < 0.5:  # staged split rows
+                p["config"]["split"] = r.choice([2, 4, 8])
     return p
 
 
@@ -72,9 +75,7 @@ def _inputs(p: dict) -> dict:
                              with_bias=p["with_bias"], with_addend=p["with_addend"])
 
 
-@pytest.mark.parametrize("i", range(CASES))
-def test_random_problem(i):
-    p = _draw(i)
+def _check(p: dict) -> None:
     inp = _inputs(p)
     kw = dict(config=p["config"], inplace=p["inplace"], partial_scale=p["partial_scale"],
               scale_layout=p["scale_layout"], schedule=p["schedule"])
@@ -94,6 +95,21 @@ def test_random_problem(i):
     compare(a, ref, inp)
 
 
+@pytest.mark.parametrize("i", range(CASES))
+def test_random_problem(i):
+    _check(_draw(i))
+
+
+@pytest.mark.parametrize("i", range(SLICE_CASES))
+def test_random_staged_split_rows(i):
+    """Random problems forced onto the staged kernel with rows split across a cluster."""
+    p = _draw(CASES + i)
+    r = random.Random(31 * i + 5)
+    p["config"] = dict(kernel=0, vec_per_thread=1, ctas_per_sm=8, stages=0,
+                       split=r.choice([2, 4, 8]))
+    _check(p)
+
+
 def test_draws_cover_every_mode_and_option():
     """The seeded draws include every mode, each option, forced launches and in-place updates."""
     ps = [_draw(i) for i in range(CASES)]
@@ -110,6 +126,9 @@ def test_draws_cover_every_mode_and_option():
     splits = [p for p in ps if p["config"] and p["config"].get("split", 0) > 1]
     assert {p["config"]["split"] for p in splits} == {2, 4, 8}
     assert {p["mode"] for p in splits} == set(MODES)
+    staged_splits = [p for p in splits if p["config"]["kernel"] == 0]
+    assert {p["config"]["split"] for p in staged_splits} == {2, 4, 8}
+    assert len({p["mode"] for p in staged_splits}) >= 3
     assert any(p["scale_layout"] == 1 for p in splits)
     assert any(p["config"] and p["with_addend"] for p in ps)
 
