@@ -169,13 +169,17 @@ sp_status sp_check_args(const void* partials, int tp, int64_t T_pad, int64_t T_v
  *                  the library's device memory (no allocation): one slot per stream (told apart
  *                  by cudaStreamGetId), reset by each call's last CTA, so calls on one stream
  *                  reuse it in stream order and calls on different streams never share one.
- *                  Slots are held for the life of the process: a process that has used 256
- *                  streams on a device runs the static schedule on every later stream (same
- *                  results, up to ~13 % slower on large calls) unless it passes row_counter. A
- *                  call also falls back to the static schedule while its stream is being
- *                  captured into a CUDA graph (a replay may run beside calls on the capturing
- *                  stream), again unless it passes row_counter. sp_last_launch tells which
- *                  schedule a call ran. Any other value is SP_ERR_UNSUPPORTED.
+ *                  Once all 256 are taken, a call on a new stream takes over the least
+ *                  recently used idle slot: one whose launches have all finished with it (each
+ *                  launch records that in the library's device memory; the library reads the
+ *                  table back on a non-blocking stream of its own, created the first time, only
+ *                  when a new stream finds the table full). Only while every slot still has a
+ *                  launch queued or claiming rows does a call on a new stream run the static
+ *                  schedule (same results, up to ~13 % slower on large calls), unless it passes
+ *                  row_counter. A call also falls back to the static schedule while its stream
+ *                  is being captured into a CUDA graph (a replay may run beside calls on the
+ *                  capturing stream), again unless it passes row_counter. sp_last_launch tells
+ *                  which schedule a call ran. Any other value is SP_ERR_UNSUPPORTED.
  *   launch         a launch configuration (below) to run instead of the one sp_select_launch
  *                  picks, for tests and tuning; NULL (the default) = the library's choice. The
  *                  checks of sp_fused_reduce_norm_with_config apply. With host_buffers = 1 it

@@ -52,6 +52,8 @@ struct Params {
   uint64_t wait_limit_ns;     // every bounded wait gives up after this long
   int64_t withhold;           // self-test only: CTA 0 skips its ring fill of this issue number
   int split_chunk;            // split rows: 16-byte vectors of a row per CTA of the cluster
+  unsigned long long* slot_done;  // dynamic schedule on a slot of the library's counter table:
+  unsigned long long slot_seq;    // where and what the launch writes once it has reset the slot
 };
 
 

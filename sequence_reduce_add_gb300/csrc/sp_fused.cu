@@ -140,6 +140,17 @@ struct DeviceInfo {
   std::mutex slot_mutex;
   unsigned long long slot_stream[spk::kRowCounterSlots] = {};
   int slots_used = 0;
+  // Reclaiming slots once all are taken: launches issued on each slot (the device writes the
+  // sequence number of each finished one into spk::g_row_counter_done, at `slot_done`), calls
+  // holding a slot between choosing it and launching, the last use of each slot (for taking the
+  // least recently used), and the library's own stream and buffer for reading the table back.
+  unsigned long long* slot_done = nullptr;
+  unsigned long long slot_issued[spk::kRowCounterSlots] = {};
+  int slot_pending[spk::kRowCounterSlots] = {};
+  unsigned long long slot_tick[spk::kRowCounterSlots] = {};
+  unsigned long long tick = 0;
+  cudaStream_t reclaim_stream = nullptr;
+  unsigned long long done_read[spk::kRowCounterSlots] = {};
 };
 DeviceInfo g_devices[kMaxDevices];
 std::mutex g_devices_mutex;
@@ -157,6 +168,10 @@ sp_status device_info(DeviceInfo** info) {
       void* counters = nullptr;
       if (cudaGetSymbolAddress(&counters, spk::g_row_counters) != cudaSuccess) return SP_ERR_CUDA;
       d.counters = static_cast<unsigned int*>(counters);
+      void* slot_done = nullptr;
+      if (cudaGetSymbolAddress(&slot_done, spk::g_row_counter_done) != cudaSuccess)
+        return SP_ERR_CUDA;
+      d.slot_done = static_cast<unsigned long long*>(slot_done);
       void* error_word = nullptr;
       if (cudaGetSymbolAddress(&error_word, spk::g_error_flags) != cudaSuccess) return SP_ERR_CUDA;
       d.error_word = static_cast<unsigned int*>(error_word);
@@ -179,10 +194,38 @@ constexpr int64_t kDynamicMinRowsPerCta = 10;
 constexpr int64_t kDynamicMinHidden = 2048;
 constexpr int64_t kDynamicMinRowBytes = 24 * 1024;
 
+// The least recently used idle slot, or -1. Called with the slot mutex held, once every slot is
+// taken. A slot is idle when no call holds it and every launch issued on it has reset it (the
+// table the launches write is read back on the library's own non-blocking stream, which waits
+// for no other work; this costs a few microseconds and happens only when a new stream finds the
+// table full). The slot's counters are then zero, and launches still finishing their last rows
+// no longer touch them.
+int reclaim_slot(DeviceInfo* dev) {
+  if (dev->reclaim_stream == nullptr &&
+      cudaStreamCreateWithFlags(&dev->reclaim_stream, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    dev->reclaim_stream = nullptr;
+    return -1;
+  }
+  if (cudaMemcpyAsync(dev->done_read, dev->slot_done, sizeof(dev->done_read),
+                      cudaMemcpyDeviceToHost, dev->reclaim_stream) != cudaSuccess ||
+      cudaStreamSynchronize(dev->reclaim_stream) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  int best = -1;
+  for (int i = 0; i < dev->slots_used; ++i)
+    if (dev->slot_pending[i] == 0 && dev->done_read[i] == dev->slot_issued[i] &&
+        (best < 0 || dev->slot_tick[i] < dev->slot_tick[best]))
+      best = i;
+  return best;
+}
+
 // Row counter slot of `stream` on this device, or -1: the call then uses the static schedule.
 // No slot while the stream is being captured (a replay of the graph may run beside later calls
-// on the same stream) or once every slot is taken.
-int counter_slot(DeviceInfo* dev, cudaStream_t stream) {
+// on the same stream), nor when every slot is taken and none is idle. `*seq` receives the
+// launch's sequence number on the slot; the call hands the slot back with release_slot.
+int counter_slot(DeviceInfo* dev, cudaStream_t stream, unsigned long long* seq) {
   cudaStreamCaptureStatus capture = cudaStreamCaptureStatusNone;
   if (cudaStreamIsCapturing(stream, &capture) != cudaSuccess) {
     cudaGetLastError();
@@ -195,11 +238,26 @@ int counter_slot(DeviceInfo* dev, cudaStream_t stream) {
     return -1;
   }
   std::lock_guard<std::mutex> lock(dev->slot_mutex);
-  for (int i = 0; i < dev->slots_used; ++i)
-    if (dev->slot_stream[i] == id) return i;
-  if (dev->slots_used == spk::kRowCounterSlots) return -1;
-  dev->slot_stream[dev->slots_used] = id;
-  return dev->slots_used++;
+  int slot = -1;
+  for (int i = 0; i < dev->slots_used && slot < 0; ++i)
+    if (dev->slot_stream[i] == id) slot = i;
+  if (slot < 0) slot = dev->slots_used < spk::kRowCounterSlots ? dev->slots_used++
+                                                                 : reclaim_slot(dev);
+  if (slot < 0) return -1;
+  dev->slot_stream[slot] = id;
+  dev->slot_tick[slot] = ++dev->tick;
+  ++dev->slot_pending[slot];
+  *seq = ++dev->slot_issued[slot];
+  return slot;
+}
+
+// Hands back a slot that counter_slot gave. A launch that was not issued takes its sequence
+// number back if no later call took one (else the slot stays busy until a later launch on it
+// has finished).
+void release_slot(DeviceInfo* dev, int slot, unsigned long long seq, bool launched) {
+  std::lock_guard<std::mutex> lock(dev->slot_mutex);
+  if (!launched && dev->slot_issued[slot] == seq) --dev->slot_issued[slot];
+  --dev->slot_pending[slot];
 }
 
 int consumer_threads(int64_t H, int vec) {
@@ -489,6 +547,8 @@ cudaError_t launch_one(const sp_launch_config& cfg, spk::Params& p, int smem, co
                       dev, &grid);
   if (e != cudaSuccess) return e;
   unsigned int* counter = nullptr;
+  int slot = -1;  // this call's slot of the library's row counter table, if it took one
+  unsigned long long seq = 0;
   const bool want_dynamic =
       schedule == SP_SCHEDULE_DYNAMIC ||
       (schedule == SP_SCHEDULE_AUTO && p.rows_total >= kDynamicMinRowsPerCta * grid &&
@@ -500,8 +560,12 @@ cudaError_t launch_one(const sp_launch_config& cfg, spk::Params& p, int smem, co
     if (x.row_counter) {
       counter = static_cast<unsigned int*>(x.row_counter);
     } else {
-      const int slot = counter_slot(dev, stream);
-      if (slot >= 0) counter = dev->counters + 2 * slot;
+      slot = counter_slot(dev, stream, &seq);
+      if (slot >= 0) {
+        counter = dev->counters + 2 * slot;
+        p.slot_done = dev->slot_done + slot;
+        p.slot_seq = seq;
+      }
     }
   }
   if (counter) {
@@ -511,21 +575,24 @@ cudaError_t launch_one(const sp_launch_config& cfg, spk::Params& p, int smem, co
     if (e == cudaSuccess)
       e = persistent_grid(spk::k_staged<kVec, kMode, true>, threads, smem, cfg.ctas_per_sm,
                           p.T_pad, dev, &grid);
-    if (e != cudaSuccess) return e;
     p.row_counter = counter;
   }
   void (*kernel)(spk::Params) =
       counter ? spk::k_staged<kVec, kMode, true> : spk::k_staged<kVec, kMode, false>;
   if constexpr (kVec == 2) {
-    if (x.withhold >= 0) {  // the self-test's instantiation (two vectors per thread only)
+    // the self-test's instantiation (two vectors per thread only)
+    if (e == cudaSuccess && x.withhold >= 0) {
       kernel = counter ? spk::k_staged<kVec, kMode, true, true>
                        : spk::k_staged<kVec, kMode, false, true>;
       e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                kSmemPerCtaMax);
-      if (e != cudaSuccess) return e;
     }
   }
-  e = launch_pdl(kernel, grid, threads, smem, stream, p);
+  // From here on a slot taken above is handed back on every path.
+  const bool ready = e == cudaSuccess;
+  if (ready) e = launch_pdl(kernel, grid, threads, smem, stream, p);
+  if (slot >= 0) release_slot(dev, slot, seq, ready && e == cudaSuccess);
+  if (!ready) return e;
   t_last_launch.grid = grid;
   t_last_launch.schedule = counter ? SP_SCHEDULE_DYNAMIC : SP_SCHEDULE_STATIC;
   return e != cudaSuccess ? e : cudaGetLastError();

@@ -38,6 +38,10 @@ constexpr int kProducerThreads = 32;
 // (which starts claiming only after this one has completed) finds it zeroed.
 constexpr int kRowCounterSlots = 256;
 __device__ unsigned int g_row_counters[2 * kRowCounterSlots];
+// Per slot, the sequence number of the last launch on it that has reset it (written by that
+// launch's last CTA to finish claiming, after the reset). The host compares it with the number of
+// launches it issued on the slot to tell when the slot is idle and may go to another stream.
+__device__ unsigned long long g_row_counter_done[kRowCounterSlots];
 
 // The CTA's error word address, kept in shared memory beside the abort flag: a report site (a
 // cold path inside the row loops) reads it there instead of holding it in registers.
@@ -187,6 +191,7 @@ __global__ void __launch_bounds__(kMaxConsumerThreads + kProducerThreads)
         counter[0] = 0u;
         counter[1] = 0u;
         __threadfence();
+        if (p.slot_done) *reinterpret_cast<volatile unsigned long long*>(p.slot_done) = p.slot_seq;
       }
     }
     return;

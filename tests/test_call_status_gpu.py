@@ -148,10 +148,11 @@ def test_selftest_rejects_bad_arguments():
 
 
 def test_caller_row_counter_on_streams_beyond_the_table():
-    """More streams than the table's 256 slots: without a counter of its own a later stream runs
-    the static schedule (sp_last_launch shows it); with one it runs the dynamic schedule. Both
-    give the same bytes, and the caller's counter is zero again afterwards. Runs in a child
-    process, so that this process's table keeps free slots for the other tests."""
+    """More streams than the table's 256 slots: once the earlier streams' calls are done, a later
+    stream takes over an idle slot and runs the dynamic schedule (sp_last_launch shows it) on a
+    call that claims many rows from that slot; with a counter of its own it runs the dynamic
+    schedule too. Both give the same bytes, and the caller's counter is zero again afterwards.
+    Runs in a child process, so that this process's table is left as it was."""
     here = os.path.dirname(os.path.abspath(__file__))
     env = dict(os.environ, PYTHONPATH=os.pathsep.join(
         [os.path.dirname(here), here, os.environ.get("PYTHONPATH", "")]))
@@ -180,8 +181,9 @@ def _streams_beyond_the_table():
         last = handles[-1]
         a = sp.allocate_outputs(inp["T_pad"], inp["H"], inp["mode"], DEV)
         _call(inp, a, sp.sp_options_init(schedule="dynamic"), stream=last)
-        assert sp.sp_last_launch()["schedule"] == "static"
+        assert sp.sp_last_launch()["schedule"] == "dynamic"  # a reclaimed slot
         counter = _words(4)
+        torch.cuda.synchronize()  # the counter's zeros written before `last` reads them
         b = sp.allocate_outputs(inp["T_pad"], inp["H"], inp["mode"], DEV)
         _call(inp, b, sp.sp_options_init(schedule="dynamic", row_counter=counter), stream=last)
         assert sp.sp_last_launch()["schedule"] == "dynamic"

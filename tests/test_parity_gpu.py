@@ -392,8 +392,11 @@ def test_dynamic_schedule_on_two_streams_concurrently():
 
 
 def test_dynamic_schedule_with_more_streams_than_counter_slots():
-    """Streams beyond the counter table fall back to the static schedule: still correct. Runs in a
-    child process, so that this process's table keeps free slots for the other tests."""
+    """Streams beyond the 256-slot counter table take over idle slots: after 256 streams have
+    each made a call and the device is idle, 44 new streams still run the dynamic schedule, with
+    the same bytes. Then 300 more streams call without waiting, so that new streams find the
+    table full while slots are busy (those calls may run either schedule; the bytes must not
+    change). Runs in a child process, so that this process's table is left as it was."""
     import os
     import subprocess
     import sys
@@ -409,15 +412,28 @@ def test_dynamic_schedule_with_more_streams_than_counter_slots():
 def _more_streams_than_counter_slots():
     w = synth.workload(2)
     inp = _small(w, rows=64)
-    outs = [sp.allocate_outputs(inp["T_pad"], inp["H"], inp["mode"], DEV) for _ in range(300)]
-    # 300 distinct CUDA streams (torch's stream pool would hand out the same few again)
-    raw = [torch.cuda.ExternalStream(_new_raw_stream()) for _ in range(300)]
+    n_first, n_reclaim, n_busy = 256, 44, 300
+    n = n_first + n_reclaim + n_busy
+    outs = [sp.allocate_outputs(inp["T_pad"], inp["H"], inp["mode"], DEV) for _ in range(n)]
+    # distinct CUDA streams (torch's stream pool would hand out the same few again)
+    raw = [torch.cuda.ExternalStream(_new_raw_stream()) for _ in range(n)]
     torch.cuda.synchronize()
-    for o, st in zip(outs, raw):
-        _call_ex(inp, o, stream=st, schedule="dynamic")
+    staged = sp.sp_options_init(schedule="dynamic", launch=dict(
+        kernel=0, vec_per_thread=2, ctas_per_sm=1, stages=0))  # the kernel with the schedule
+    schedules = []
+    for i, (o, st) in enumerate(zip(outs, raw)):
+        if i in (n_first, n_first + n_reclaim):
+            torch.cuda.synchronize()  # every slot idle
+        sp.sp_fused_reduce_norm_ex(staged, inp["partials"], inp["weight"], o["out"],
+                                   o["residual_out"], residual=inp["residual"], bias=inp["bias"],
+                                   eps=inp["eps"], quant_mode=inp["mode"],
+                                   out_scales=o["out_scales"], T_valid=inp["T_valid"], stream=st)
+        schedules.append(sp.sp_last_launch()["schedule"])
     torch.cuda.synchronize()
+    assert schedules[:n_first + n_reclaim] == ["dynamic"] * (n_first + n_reclaim), schedules
+    assert set(schedules[n_first + n_reclaim:]) <= {"dynamic", "static"}
     ref = run_oracle(inp)
-    for o in (outs[0], outs[150], outs[299]):
+    for o in (outs[0], outs[n_first], outs[n - 1]):
         compare(_host(o), ref, inp)
     first = _host(outs[0])
     for o in outs[1:]:
@@ -426,7 +442,7 @@ def _more_streams_than_counter_slots():
             assert np.array_equal(h[k].view(np.uint8), first[k].view(np.uint8))
     for st in raw:
         _destroy_raw_stream(st.cuda_stream)
-    print("streams ok")
+    print("streams ok", schedules[n_first + n_reclaim:].count("static"), "static of", n_busy)
 
 
 def _cudart():
