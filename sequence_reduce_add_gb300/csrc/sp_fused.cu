@@ -773,8 +773,8 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   //                     (NVFP4 from H = 4609); tp >= 12, 8 up to 16 rows (4 below H = 7168) and
   //                     4 up to 64 (2 for 33-64 rows at H <= 5120, not for NVFP4), 4 for 65-80
   //                     rows at H >= 7168 and for 65-96 at H <= 5120 (NVFP4 from H = 4609, and
-  //                     up to 128 rows). Then direct with two vectors per thread up to 128 rows (160 at
-  //                     tp <= 3 and H >= 7168; at tp >= 12 up to 96, or 128 below H = 8192:
+  //                     up to 128 rows). Then direct with two vectors per thread up to 128 rows
+  //                     (160 at tp <= 3 and H >= 7168; at tp >= 12 up to 96, or 128 below 8192:
   //                     15-36 % faster than the one-CTA-per-SM deep ring it replaced), split 2 up
   //                     to 224 rows at H = 5120, and at H 5121-6144 (tp < 12) split 2 up to 152
   //                     rows (NVFP4: 4) and 4 up to 160; at H >= 7168, 129-144 rows split 4 for
@@ -807,11 +807,11 @@ sp_status sp_select_launch(int tp, int64_t T_pad, int64_t H, int quant_mode,
   // bound (T 128-512, H 2048-8192) gave two more bands: 4 CTAs per row for 97-128 rows at
   // 4096 < H <= 5120 and tp >= 6 (3-7 % faster on L2-resident inputs, 4-17 % from HBM), and 2
   // per row for NVFP4 output past 128 rows in the direct band at H >= 3072 (1-24 % and up to
-  // 38 % faster); the others it suggested were slower on L2-resident inputs and left out. Over 195 swept shapes
-  // (tp 2-16, H 4096-16384, T 16-320) 1.5 % faster summed, none slower; against the previous
-  // rule 8-38 % faster on L2-resident inputs (tp 8, H 8192, 160 rows: 8.31 -> 5.18 µs); on
-  // inputs from HBM 7-37 % faster at H = 4096, -9 to +1 % at tp 8 and H >= 7168, and 4-11 %
-  // slower at tp <= 5.
+  // 38 % faster); the others it suggested were slower on L2-resident inputs and left out. The
+  // staged split rows, over 195 swept shapes (tp 2-16, H 4096-16384, T 16-320): 1.5 % faster
+  // summed, none slower; against the previous rule 8-38 % faster on L2-resident inputs (tp 8,
+  // H 8192, 160 rows: 8.31 -> 5.18 µs); on inputs from HBM 7-37 % faster at H = 4096, -9 to
+  // +1 % at tp 8 and H >= 7168, and 4-11 % slower at tp <= 5.
   const int64_t elems = static_cast<int64_t>(tp) * T_pad * H;
   const int64_t rows_x_h = T_pad * H;
   bool direct = false;
