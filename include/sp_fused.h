@@ -267,7 +267,8 @@ sp_status sp_fused_reduce_norm_host(const void* partials, int tp, int64_t T_pad,
  * tensors of the call, and latency-critical serving loops that forbid allocation after start-up
  * (cudaMalloc can synchronise the device and take milliseconds). Such a caller cannot provide
  * the 8-byte row counter that the dynamic row schedule needs (sp_fused_options.row_counter), and
- * the library's per-stream counter table serves only the first 256 streams of a process. This
+ * the library's per-stream counter table serves no call under graph capture and at most 256
+ * streams with launches in flight at once. This
  * entry point keeps that counter in an array of the library's own static device memory instead:
  * 8 bytes, one array per GPU that loads the library, held until the process exits, shared by
  * every call of this entry point. The caller passes exactly the buffers of sp_fused_reduce_norm.
