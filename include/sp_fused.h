@@ -31,12 +31,15 @@
  *     the argument says "host". The caller owns every buffer; the library allocates nothing and
  *     may be called concurrently from several host threads. What it keeps between calls is
  *     listed where it is used: the device error word (sp_device_error), the dynamic row
- *     schedule's per-stream counters (sp_fused_options.row_counter), the no-allocation entry's
- *     counter (sp_fused_reduce_norm_noalloc) and each host thread's last launch (sp_last_launch).
+ *     schedule's per-stream counters with their completion numbers and the one stream it creates
+ *     to read those back (sp_fused_options.schedule), the no-allocation entry's counter
+ *     (sp_fused_reduce_norm_noalloc) and each host thread's last launch (sp_last_launch).
  *   - bf16 is IEEE binary32's top 16 bits; FP8 E4M3 is the OCP "E4M3" (fn) format; E2M1 is the
  *     OCP MX FP4 format. All tensors are dense, row-major, C-contiguous.
  *   - Calls are asynchronous on `stream` (NULL = legacy default stream); nothing synchronises the
- *     host. Errors found before the launch leave every buffer untouched.
+ *     host, except that a dynamic-schedule call on a new stream that finds all 256 counter slots
+ *     taken waits for a 2 KB read on the library's own stream (sp_fused_options.schedule).
+ *     Errors found before the launch leave every buffer untouched.
  */
 #ifndef SP_FUSED_H
 #define SP_FUSED_H
