@@ -201,18 +201,27 @@ constexpr int64_t kDynamicMinRowBytes = 24 * 1024;
 // table full). The slot's counters are then zero, and launches still finishing their last rows
 // no longer touch them.
 int reclaim_slot(DeviceInfo* dev) {
+  // This thread's capture mode is relaxed for the read, so that a CUDA graph being recorded by
+  // another thread in global mode neither refuses these calls nor is invalidated by them (the
+  // calling stream itself is not being captured: counter_slot checked).
+  cudaStreamCaptureMode mode = cudaStreamCaptureModeRelaxed;
+  if (cudaThreadExchangeStreamCaptureMode(&mode) != cudaSuccess) {
+    cudaGetLastError();
+    return -1;
+  }
+  bool read = true;
   if (dev->reclaim_stream == nullptr &&
       cudaStreamCreateWithFlags(&dev->reclaim_stream, cudaStreamNonBlocking) != cudaSuccess) {
-    cudaGetLastError();
     dev->reclaim_stream = nullptr;
-    return -1;
+    read = false;
   }
-  if (cudaMemcpyAsync(dev->done_read, dev->slot_done, sizeof(dev->done_read),
-                      cudaMemcpyDeviceToHost, dev->reclaim_stream) != cudaSuccess ||
-      cudaStreamSynchronize(dev->reclaim_stream) != cudaSuccess) {
-    cudaGetLastError();
-    return -1;
-  }
+  read = read &&
+         cudaMemcpyAsync(dev->done_read, dev->slot_done, sizeof(dev->done_read),
+                         cudaMemcpyDeviceToHost, dev->reclaim_stream) == cudaSuccess &&
+         cudaStreamSynchronize(dev->reclaim_stream) == cudaSuccess;
+  if (!read) cudaGetLastError();
+  cudaThreadExchangeStreamCaptureMode(&mode);  // back to the thread's own mode
+  if (!read) return -1;
   int best = -1;
   for (int i = 0; i < dev->slots_used; ++i)
     if (dev->slot_pending[i] == 0 && dev->done_read[i] == dev->slot_issued[i] &&

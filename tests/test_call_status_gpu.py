@@ -11,7 +11,8 @@ the GPU and without a fault.
   withholding a segment mid-row exercises the segment waits' vote.
 * A caller's own row counter (options.row_counter) gives the dynamic schedule on any stream and
   inside a captured graph; sp_last_launch tells which schedule a call ran, so the per-stream
-  table's fallback is visible.
+  table's behaviour is visible: beyond its 256 slots a new stream takes over an idle slot, also
+  while another host thread records a graph.
 """
 import ctypes
 import os
@@ -200,6 +201,87 @@ def _streams_beyond_the_table():
     print("streams ok")
 
 
+def test_slot_reclaimed_while_another_thread_records_a_graph():
+    """A call on a new stream that finds the counter table full reads the table back on the
+    library's own stream. Made while another host thread records a CUDA graph in global capture
+    mode (PyTorch's default), that read must neither fail nor break the recording: the call runs
+    the dynamic schedule on a reclaimed slot and matches the oracle, and the graph, which holds
+    a fused call of its own, replays to the oracle's result. Runs in a child process (it fills the
+    table)."""
+    here = os.path.dirname(os.path.abspath(__file__))
+    env = dict(os.environ, PYTHONPATH=os.pathsep.join(
+        [os.path.dirname(here), here, os.environ.get("PYTHONPATH", "")]))
+    proc = subprocess.run([sys.executable, os.path.abspath(__file__), "capture"], cwd=here,
+                          env=env, capture_output=True, text=True, timeout=600)
+    assert proc.returncode == 0, proc.stdout[-2000:] + proc.stderr[-2000:]
+    assert "capture ok" in proc.stdout
+
+
+def _reclaim_during_capture():
+    import threading
+    rt = _cudart()
+    handles = []
+    for _ in range(257):
+        h = ctypes.c_void_p()
+        assert rt.cudaStreamCreateWithFlags(ctypes.byref(h), 1) == 0
+        handles.append(h.value)
+    try:
+        w = synth.workload(2)
+        small = _small(w, rows=64)
+        so = sp.allocate_outputs(small["T_pad"], small["H"], small["mode"], DEV)
+        big = _small(w, rows=2048)
+        bo = sp.allocate_outputs(big["T_pad"], big["H"], big["mode"], DEV)
+        cap = _small(synth.workload(4), rows=330)
+        co = sp.allocate_outputs(cap["T_pad"], cap["H"], cap["mode"], DEV)
+        cap_stream = torch.cuda.Stream(device=DEV)
+        dynamic, default = sp.sp_options_init(schedule="dynamic"), sp.sp_options_init()
+        torch.cuda.synchronize()
+        staged = sp.sp_options_init(schedule="dynamic", launch=dict(
+            kernel=0, vec_per_thread=2, ctas_per_sm=1, stages=0))
+        for h in handles[:256]:  # every slot of the table taken
+            _call(small, so, staged, stream=h)
+        _call(big, bo, dynamic, stream=handles[0])  # the big call's launch set up beforehand
+        with torch.cuda.stream(cap_stream):
+            _call(cap, co, default)  # and the captured call's
+        torch.cuda.synchronize()  # every slot idle
+        g = torch.cuda.CUDAGraph()
+        inside, done, seen = threading.Event(), threading.Event(), {}
+
+        def record():
+            try:
+                with torch.cuda.graph(g, stream=cap_stream):
+                    _call(cap, co, default)
+                    inside.set()
+                    assert done.wait(120)
+            except BaseException as e:  # reported by the main thread
+                seen["error"] = e
+                inside.set()
+
+        t = threading.Thread(target=record)
+        t.start()
+        assert inside.wait(120)
+        _call(big, bo, dynamic, stream=handles[256])
+        schedule = sp.sp_last_launch()["schedule"]
+        done.set()
+        t.join(120)
+        assert not t.is_alive()
+        assert "error" not in seen, seen.get("error")
+        assert schedule == "dynamic", schedule
+        torch.cuda.synchronize()
+        compare(_host(bo), run_oracle(big), big)
+        for o in co.values():
+            if o is not None:
+                o.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        compare(_host(co), run_oracle(cap), cap)
+    finally:
+        torch.cuda.synchronize()
+        for h in handles:
+            rt.cudaStreamDestroy(ctypes.c_void_p(h))
+    print("capture ok")
+
+
 def test_caller_row_counter_inside_a_captured_graph():
     """With its own counter a call keeps the dynamic schedule while its stream is captured; the
     graph replayed three times on refilled inputs gives the oracle's result each time."""
@@ -255,3 +337,5 @@ def _cudart():
 
 if __name__ == "__main__" and sys.argv[1:] == ["streams"]:
     _streams_beyond_the_table()
+if __name__ == "__main__" and sys.argv[1:] == ["capture"]:
+    _reclaim_during_capture()
