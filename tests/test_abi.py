@@ -443,11 +443,12 @@ def test_every_selected_launch_passes_the_launch_checks(lib):
     checked = 0
     for mode in ("none", "fp8_static", "fp8_per_token", "nvfp4"):
         for tp in (1, 2, 3, 4, 5, 6, 8, 12, 16, 24, 32):
-            for H in (8, 16, 24, 512, 1000, 1024, 2048, 2056, 4096, 5120, 7168, 8192, 12288,
-                      16376, 16384):
+            for H in (8, 16, 24, 512, 1000, 1024, 2048, 2056, 3072, 4096, 4608, 5120, 6144,
+                      7168, 8192, 12288, 16376, 16384):
                 if mode == "nvfp4" and H % 16:
                     continue
-                for T in (1, 2, 7, 8, 16, 33, 64, 100, 128, 152, 256, 304, 500, 1024, 4096, 9999):
+                for T in (1, 2, 7, 8, 16, 24, 32, 33, 48, 64, 80, 96, 100, 120, 128, 144, 152,
+                          160, 192, 224, 256, 304, 500, 1024, 4096, 9999):
                     T_pad = sp.sp_pad_tokens(T, tp)
                     cfg = sp.sp_select_launch(tp, T_pad, H, mode)
                     o = sp.Options()
